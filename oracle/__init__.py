@@ -1,0 +1,142 @@
+"""CPU oracle for CSR SpMM (sum, mean, max + argmax) -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The CUDA library never calls it; the two
+share no code. The arithmetic lives in ``spmm_oracle.c`` (fp64 accumulation per
+row in CSR order); this module compiles it with gcc on first use and wraps it
+with ctypes.
+
+Semantics (graph-spmm model card, "API" and "Correctness"; ParamSpMM
+section 2, Algorithm 1):
+
+* ``sum``  C[i,k] = sum over stored entries p of row i of a_p * B[col_p, k]
+* ``mean`` the sum divided by the number of stored entries of row i; empty -> 0
+* ``max``  max over the fp32-rounded products, ties to the smallest column;
+           empty -> (0, -1)
+
+``T`` (returned for sum/mean) is sum_p |a_p * B[col_p, k]|, the scale of the
+tolerance |err| <= 1e-5 * T + 1e-6.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spmm_oracle.c")
+_LIB = os.path.join(_HERE, "libspmm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+REDUCE = {"sum": 0, "mean": 1, "max": 2}
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("nnz", ctypes.c_int64), ("d_max", ctypes.c_int64),
+                ("n_empty", ctypes.c_int64), ("dbar", ctypes.c_double), ("cv", ctypes.c_double)]
+
+
+def _compile(out: str, defines=()) -> None:
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC"]
+    cmd += [f"-D{d}" for d in defines]
+    subprocess.run(cmd + ["-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, out)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle library (plain C, OpenMP, no FP contraction)."""
+    with _lock:
+        fresh = os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)
+        if force or not fresh:
+            _compile(_LIB)
+    return _LIB
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """ctypes view of one build of spmm_oracle.c."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        p = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        lib.oracle_spmm_rows.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int, p, i64, p, p, p]
+        lib.oracle_spmm_rows.restype = ctypes.c_int
+        lib.oracle_descriptors.argtypes = [i64, p, ctypes.POINTER(_Desc)]
+        lib.oracle_descriptors.restype = ctypes.c_int
+        lib.oracle_threads.restype = ctypes.c_int
+        self.lib = lib
+
+    def threads(self) -> int:
+        return int(self.lib.oracle_threads())
+
+    def spmm(self, rowptr, col, val, B, reduce: str, rows=None, K=None):
+        rowptr = np.ascontiguousarray(rowptr, dtype=np.int32)
+        col = np.ascontiguousarray(col, dtype=np.int32)
+        val = None if val is None else np.ascontiguousarray(val, dtype=np.float32)
+        B = np.ascontiguousarray(B, dtype=np.float32)
+        if B.ndim != 2:
+            raise ValueError("B must be 2-D")
+        M = len(rowptr) - 1
+        K = B.shape[0] if K is None else K
+        N = B.shape[1]
+        if rows is None:
+            R, rows_arr = M, None
+        else:
+            rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+            R = len(rows_arr)
+        red = REDUCE[reduce]
+        C = np.empty((R, N), dtype=np.float32)
+        A = np.empty((R, N), dtype=np.int32) if red == 2 else None
+        T = np.empty((R, N), dtype=np.float32) if red != 2 else None
+        rc = self.lib.oracle_spmm_rows(M, K, N, _ptr(rowptr), _ptr(col), _ptr(val), _ptr(B), red,
+                                       _ptr(rows_arr), R, _ptr(C), _ptr(A), _ptr(T))
+        if rc != 0:
+            raise ValueError("oracle_spmm_rows rejected its arguments")
+        return C, A, T
+
+    def descriptors(self, rowptr) -> dict:
+        rowptr = np.ascontiguousarray(rowptr, dtype=np.int32)
+        d = _Desc()
+        if self.lib.oracle_descriptors(len(rowptr) - 1, _ptr(rowptr), ctypes.byref(d)) != 0:
+            raise ValueError("invalid row pointers")
+        return dict(M=d.M, nnz=d.nnz, d_max=d.d_max, n_empty=d.n_empty, dbar=d.dbar, cv=d.cv)
+
+
+def planted(n: int, out_dir: str) -> Oracle:
+    """A build with planted mistake n (1..5), for the tests that check the pins."""
+    out = os.path.join(out_dir, f"libspmm_oracle_plant{n}.so")
+    _compile(out, [f"ORACLE_PLANT={n}"])
+    return Oracle(out)
+
+
+def _default() -> Oracle:
+    global _lib
+    if _lib is None:
+        _lib = Oracle(build())
+    return _lib
+
+
+def threads() -> int:
+    return _default().threads()
+
+
+def spmm(rowptr, col, val, B, reduce: str, rows=None, K=None):
+    """Oracle SpMM. Returns (C float32 [R,N], argmax int32 [R,N] or None, T float32 [R,N] or None).
+
+    ``rows`` selects output rows (int64 array); None means all M rows.
+    """
+    return _default().spmm(rowptr, col, val, B, reduce, rows, K)
+
+
+def descriptors(rowptr) -> dict:
+    """M, nnz, d_max, n_empty, dbar = nnz/M, cv = std(d)/mean(d) over all rows."""
+    return _default().descriptors(rowptr)
