@@ -1,0 +1,396 @@
+"""Benchmark of the CSR SpMM engine on one GB300 (or N independent replicas).
+
+A step is one pass of the hot path over the workload: one spmm_run per
+(N, reduce) pair the workload lists, each preceded by an L2 flush (a write of
+twice the L2 size) so that every timed launch reads its inputs from HBM. The
+plan (descriptors, heavy-row tables, workspace) is built before timing, as a
+GNN layer reuses it. Device time comes from CUDA events around each run on
+the launching stream; value = sum of 2*nnz*N over the timed runs / that time.
+
+Default workload: kNN/road-like locality graph, M = K = 1,048,576, 10 distinct
+neighbours within +-512 of the row id, unweighted, N in {16, 64}, sum and mean.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+``--impl reference`` times the CPU oracle (the slow, plain fp64 program the
+CUDA path is checked against) on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import json
+import os
+import shutil
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel and the
+# workload; None until a capture of the current kernel exists.
+NCU_TRAFFIC = {}
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--family", default="auto", choices=["auto", "rowgroup", "warprow", "coltile"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload(cid):
+    import gen
+    spec = gen.CONFIGS[cid]
+    g = gen.config(cid)
+    runs = [(n, r) for n in spec["N"] for r in spec["reduce"]]
+    return spec, g, runs
+
+
+def compulsory_bytes(g, N, reduce):
+    """rowptr + col + val + B read once + C written (+ argmax for max)."""
+    b = 4 * (g.M + 1) + 4 * g.nnz + (4 * g.nnz if g.val is not None else 0)
+    b += 4 * g.K * N + 4 * g.M * N
+    if reduce == "max":
+        b += 4 * g.M * N
+    return b
+
+
+def describe_workload(spec, g, runs):
+    return (f"{spec['name']}: M={g.M:,} K={g.K:,} nnz={g.nnz:,} "
+            f"{'weighted' if g.val is not None else 'unweighted'}; "
+            f"runs per step: " + ", ".join(f"N={n} {r}" for n, r in runs))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = None
+        if shutil.which("nvidia-smi") is None:
+            return
+        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.f = open(self.path, "w")
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+             "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+            stderr=subprocess.DEVNULL)
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, n = [], None, set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if not (t0 - 0.05 <= ts <= t1 + 0.05):
+                continue
+            n += 1
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                pass
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def time_oracle(g, B_by_N, runs, rows, budget_s, min_reps=1):
+    """Oracle wall time for the given rows over all runs, repeated to fill budget_s."""
+    import oracle
+    reps, t_total = 0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        for n, r in runs:
+            oracle.spmm(g.rowptr, g.col, g.val, B_by_N[n], r, rows=rows)
+        t_total += time.perf_counter() - t0
+        reps += 1
+        if reps >= min_reps and t_total >= budget_s:
+            break
+        if reps >= min_reps and t_total / reps * (reps + 1) > 3 * budget_s:
+            break
+    return t_total / reps, reps
+
+
+def sample_rows(g, frac, seed=0):
+    n = max(1, int(round(g.M * frac)))
+    if n >= g.M:
+        return None, g.nnz
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(g.M, size=n, replace=False)).astype(np.int64)
+    deg = np.diff(g.rowptr.astype(np.int64))
+    return rows, int(deg[rows].sum())
+
+
+def cpu_leg(g, B_by_N, runs, budget_s):
+    """Size a row sample so that one pass over all runs takes about budget_s / 3."""
+    import oracle
+    probe_rows, probe_nnz = sample_rows(g, min(1.0, 20000 / max(g.M, 1)), seed=1)
+    t_probe, _ = time_oracle(g, B_by_N, runs, probe_rows, 0.0)
+    frac = min(1.0, (budget_s / 3) / max(t_probe, 1e-6) * (20000 / max(g.M, 1)))
+    rows, nnz_s = sample_rows(g, frac, seed=2)
+    t, reps = time_oracle(g, B_by_N, runs, rows, budget_s)
+    flops = sum(2.0 * nnz_s * n for n, _ in runs)
+    desc = (f"{'all' if rows is None else f'{len(rows):,} random'} rows of {g.M:,} "
+            f"({nnz_s:,} entries), every run of the step, {reps} repetition(s)")
+    return flops / t / 1e9, t, desc, oracle.threads()
+
+
+def run_reference(args):
+    world, rank, _, pg = dist_init(args)
+    if rank != 0:
+        return
+    spec, g, runs = workload(args.config)
+    import gen
+    B_by_N = {n: gen.features(g.K, n, seed=0) for n in spec["N"]}
+    # each step: a row sample sized so that W + K steps end within ~2 minutes
+    budget_total = 120.0
+    per_step = budget_total / max(1, args.steps + args.warmup)
+    import oracle
+    probe_rows, _ = sample_rows(g, min(1.0, 2000 / max(g.M, 1)), seed=1)
+    t_probe, _ = time_oracle(g, B_by_N, runs, probe_rows, 0.0)
+    frac = min(1.0, per_step / max(t_probe, 1e-6) * (2000 / max(g.M, 1)))
+    rows, nnz_s = sample_rows(g, frac, seed=3)
+    for _ in range(args.warmup):
+        for n, r in runs:
+            oracle.spmm(g.rowptr, g.col, g.val, B_by_N[n], r, rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for n, r in runs:
+            oracle.spmm(g.rowptr, g.col, g.val, B_by_N[n], r, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = sum(2.0 * nnz_s * n for n, _ in runs) * args.steps
+    value = flops / dt / 1e9
+    sample = (f"{'all' if rows is None else f'{len(rows):,} random'} rows of {g.M:,} "
+              f"({nnz_s:,} entries) per step, every run of the step")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe_workload(spec, g, runs)},
+        "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
+def run_ours(args):
+    import torch
+    world, rank, local, pg = dist_init(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import sparse_dense_matrix_gb300 as sdm
+
+    spec, g, runs = workload(args.config)
+    import gen
+    Ns = spec["N"]
+    B_host = {n: gen.features(g.K, n, seed=0) for n in Ns}
+    rowptr = torch.from_numpy(g.rowptr).to(dev)
+    col = torch.from_numpy(g.col).to(dev)
+    val = None if g.val is None else torch.from_numpy(g.val).to(dev)
+    adj = sdm.SparseAdj(rowptr, col, val, num_cols=g.K)
+    if args.family != "auto":
+        adj.set_family(args.family)
+    for n, r in runs:
+        adj.reserve(n, r)
+    Bd = {n: torch.from_numpy(B_host[n]).to(dev) for n in Ns}
+    Cd = {n: torch.empty((g.M, n), dtype=torch.float32, device=dev) for n in Ns}
+    Ad = {n: torch.empty((g.M, n), dtype=torch.int32, device=dev) for n in Ns}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one(n, r):
+        sdm.spmm_run(adj.plan, col.data_ptr(), None if val is None else val.data_ptr(),
+                     Bd[n].data_ptr(), n, sdm.REDUCE[r], Cd[n].data_ptr(),
+                     Ad[n].data_ptr() if r == "max" else None, stream)
+
+    for _ in range(args.warmup):
+        for n, r in runs:
+            flush.fill_(1.0)
+            one(n, r)
+    torch.cuda.synchronize()
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in runs] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    launches0 = sdm.spmm_launch_count()
+    t0 = time.time()
+    for s in range(args.steps):
+        for k, (n, r) in enumerate(runs):
+            flush.fill_(1.0)
+            ev[s][k][0].record(stream)
+            one(n, r)
+            ev[s][k][1].record(stream)
+    torch.cuda.synchronize()
+    if pg is not None:
+        pg.barrier()
+    t1 = time.time()
+    launches = sdm.spmm_launch_count() - launches0
+    sdm.spmm_plan_sync(adj.plan)
+    clk = clocks.stop(t0, t1)
+
+    per_run_ms = np.array([[a.elapsed_time(b) for a, b in ev[s]] for s in range(args.steps)])
+    dev_ms = float(per_run_ms.sum())
+    if pg is not None:
+        t = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        dev_ms = float(t.item())
+    flops_step = sum(2.0 * g.nnz * n for n, _ in runs)
+    value = flops_step * args.steps * world / (dev_ms / 1e3) / 1e9
+
+    hbm_peak, peak_kind = peaks()
+    # dominant kernel: the run with the largest mean device time
+    mean_ms = per_run_ms.mean(axis=0)
+    kdom = int(np.argmax(mean_ms))
+    n_dom, r_dom = runs[kdom]
+    info = adj.describe(n_dom, r_dom)
+    bytes_dom = compulsory_bytes(g, n_dom, r_dom)
+    achieved = bytes_dom / (mean_ms[kdom] / 1e3) / 1e9
+    key = f"{info['family_name']}/{spec['name']}/N{n_dom}/{r_dom}"
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": NCU_TRAFFIC.get(key),
+                "kernel": key, "peak_source": peak_kind,
+                "algorithmic_bytes_per_launch": bytes_dom,
+                "launches_per_run": info["launches"]}
+    per_run = []
+    for k, (n, r) in enumerate(runs):
+        b = compulsory_bytes(g, n, r)
+        per_run.append({"N": n, "reduce": r, "family": adj.describe(n, r)["family_name"],
+                        "ms": float(np.median(per_run_ms[:, k])),
+                        "gflops": 2.0 * g.nnz * n / (np.median(per_run_ms[:, k]) / 1e3) / 1e9,
+                        "hbm_frac": b / (np.median(per_run_ms[:, k]) / 1e3) / 1e9 / hbm_peak})
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        Bh = {n: torch.from_numpy(B_host[n]).pin_memory() for n in Ns}
+        Ch = {n: torch.empty((g.M, n), dtype=torch.float32).pin_memory() for n in Ns}
+        Ah = {n: torch.empty((g.M, n), dtype=torch.int32).pin_memory() for n in Ns}
+        h2d = sum(g.K * n * 4 for n, _ in runs)
+        d2h = sum(g.M * n * 4 * (2 if r == "max" else 1) for n, r in runs)
+        e2e_steps = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            for n, r in runs:
+                Bd[n].copy_(Bh[n], non_blocking=True)
+                res = adj.reduce(Bd[n], r, out=Cd[n], argmax=Ad[n] if r == "max" else None)
+                Ch[n].copy_(Cd[n], non_blocking=True)
+                if r == "max":
+                    Ah[n].copy_(res[1], non_blocking=True)
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b)
+        e2e = {"value": flops_step * e2e_steps * world / (e2e_ms / 1e3) / 1e9, "unit": "GFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, t, desc, cores = cpu_leg(g, B_host, runs, budget_s=15.0)
+        cpu = {"value": v, "unit": "GFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dev_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": describe_workload(spec, g, runs),
+                       "l2": "flushed (write of 2x L2) before every timed launch",
+                       "timing": "CUDA events around each spmm_run on the launching stream",
+                       "per_run": per_run},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(launches), "clocks": clk,
+            "hbm_gbs_compulsory": sum(compulsory_bytes(g, n, r) for n, r in runs) * args.steps
+            / (dev_ms / 1e3) / 1e9,
+        }
+        print(json.dumps(out))
+    adj.close()
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * spmm.h -- C ABI of the GB300 CSR SpMM engine (libspmm.so).
+ *
+ * The engine computes C = A . B for a fixed sparse M x K matrix A in CSR and a
+ * dense K x N fp32 matrix B, under a sum, mean or max reduction; max also
+ * returns the winning column (argmax). Semantics follow the graph-spmm model
+ * card ("API", "Method", "Correctness"): `val == NULL` is an unweighted
+ * adjacency, duplicate (row, col) entries are each counted, an empty row gives
+ * 0 for sum and mean and (0, -1) for max, and ties of max go to the smallest
+ * column. The row-wise CSR traversal is ParamSpMM section 2 ("Background",
+ * Algorithm 1); the plan's O(M) degree descriptors are RA-SpMM's (abstract and
+ * "routing rules": M, mean degree, degree coefficient of variation).
+ *
+ * Conventions for every call
+ *   - Pointers named "device" are CUDA device pointers of the current device;
+ *     the library never dereferences them on the host.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Work is enqueued on it; calls marked "synchronous" also wait
+ *     for it to drain before they return.
+ *   - Every call returns an spmm_status; no C++ exception crosses the ABI and
+ *     no device code traps. Argument checks happen on the host before any CUDA
+ *     call, so an invalid-argument status is returned even on a machine
+ *     without a GPU.
+ *   - The caller owns all tensors (rowptr, col, val, B, C, argmax). The plan
+ *     owns its own copy of rowptr, its heavy-row tables and its workspace.
+ *   - A plan may be used by one stream at a time (it owns one workspace).
+ *   - Results are bitwise reproducible run to run: no floating-point atomics,
+ *     every reduction order is a pure function of the plan and N.
+ */
+#ifndef GB300_SPMM_H
+#define GB300_SPMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPMM_OK = 0,
+    SPMM_ERR_INVALID_ARG = 1,   /* NULL pointer, negative size, unknown enum value      */
+    SPMM_ERR_INVALID_INPUT = 2, /* rowptr not a CSR row-pointer array; col out of range */
+    SPMM_ERR_OOM = 3,           /* device or host allocation failed                     */
+    SPMM_ERR_CUDA = 4,          /* a CUDA runtime call failed (no device, launch error)  */
+    SPMM_ERR_UNSUPPORTED = 5,   /* size beyond the int32 index range                     */
+    SPMM_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up (see spmm_plan_sync) */
+} spmm_status;
+
+/* graph-spmm model card, "API": spmm_sum / spmm_mean / spmm_max. */
+typedef enum { SPMM_SUM = 0, SPMM_MEAN = 1, SPMM_MAX = 2 } spmm_reduce;
+
+/* Kernel families the router chooses among (RA-SpMM "kernel portfolio" and
+ * "routing rules": the family is picked from the descriptors and N). */
+typedef enum {
+    SPMM_FAMILY_AUTO = -1,     /* let the router decide                                  */
+    SPMM_FAMILY_ROWGROUP = 0,  /* several rows per warp, L lanes per row (uniform degree) */
+    SPMM_FAMILY_WARPROW = 1,   /* one warp per row, lane groups split the row's entries   */
+    SPMM_FAMILY_COLTILE = 2    /* a CTA per row block, warps own 128-column tiles, col/val
+                                  staged in shared memory (wide N)                         */
+} spmm_family;
+
+typedef struct spmm_plan_s *spmm_plan_t;
+
+/* Descriptors and routing decision, filled by spmm_plan_describe / spmm_route. */
+typedef struct {
+    /* O(M) descriptors of the row-degree distribution */
+    int64_t M, K, nnz;
+    int64_t d_max;          /* largest row degree                                    */
+    int64_t n_empty;        /* rows with no entry                                    */
+    double dbar;            /* nnz / M (0 when M == 0)                               */
+    double cv;              /* std(d) / mean(d) over all M rows, divisor M (0 if nnz==0) */
+    /* heavy-row split (rows longer than t_split are cut into chunks of `chunk` entries,
+     * reduced per chunk, then combined in chunk order by a second launch) */
+    int64_t t_split;
+    int64_t chunk;
+    int64_t n_heavy;
+    int64_t n_chunks;
+    /* launch shape for the queried (N, reduce) */
+    int64_t N;
+    int32_t reduce;
+    int32_t family;         /* spmm_family actually used                             */
+    int32_t vec;            /* columns per lane load: 4 (128-bit) or 1               */
+    int32_t lanes;          /* lanes that share one entry (one per vec of columns)   */
+    int32_t rows_per_warp;  /* rows one warp owns (ROWGROUP), else 1                 */
+    int32_t col_tiles;      /* column tiles of 32*vec columns (grid dimension y)     */
+    int32_t launches;       /* kernel launches one spmm_run makes                    */
+    int32_t num_sms;        /* SM count the routing assumed                          */
+    int64_t workspace_bytes;/* device scratch spmm_run needs for this (N, reduce)    */
+} spmm_plan_info;
+
+/*
+ * spmm_plan_create -- build the reusable plan for one sparsity pattern.
+ *   rowptr : device, int32 [M+1], rowptr[0] == 0, non-decreasing. Copied into
+ *            plan-owned memory; the caller may free it after the call returns.
+ *   M, K   : rows and columns of A (M >= 0, K >= 0, both < 2^31).
+ *   stream : work is enqueued here. Synchronous.
+ *   out    : receives the plan (left NULL on error).
+ * Computes, in one pass over rowptr, the degree descriptors (M, nnz, mean
+ * degree, degree CV, max degree, empty rows) and the list of heavy rows that
+ * spmm_run splits across CTAs. Returns SPMM_ERR_INVALID_INPUT when rowptr[0]
+ * != 0 or rowptr decreases anywhere (checked on the device; no trap).
+ * (RA-SpMM abstract: descriptors in O(M); graph-spmm model card, "API":
+ * SparseAdj is held once and applied many times.)
+ */
+spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *stream,
+                             spmm_plan_t *out);
+
+/*
+ * spmm_run -- C = reduce_j A[i,j] * B[j,:] for every row i (asynchronous).
+ *   col    : device, int32 [nnz], every value in [0, K). Not checked here (use
+ *            spmm_plan_validate_cols once per graph); an out-of-range column
+ *            is undefined behaviour.
+ *   val    : device, fp32 [nnz], or NULL for an unweighted adjacency (every
+ *            stored entry is 1 and the value load is skipped).
+ *   B      : device, fp32 [K, N] row-major, contiguous.
+ *   N      : feature width, N >= 0. N == 0 or M == 0 returns SPMM_OK with no launch.
+ *   reduce : SPMM_SUM, SPMM_MEAN (divide by the row's stored-entry count,
+ *            empty row -> 0) or SPMM_MAX (max over fp32 products, ties to the
+ *            smallest column, empty row -> 0 and argmax -1).
+ *   C      : device, fp32 [M, N] row-major, written once per element.
+ *   argmax : device, int32 [M, N] (SPMM_MAX only; may be NULL to skip it).
+ * 128-bit loads are used when N % 4 == 0 and B and C are 16-byte aligned;
+ * otherwise the scalar path runs (same results). Grows the plan's workspace
+ * with cudaMalloc when the heavy-row split needs more than it holds (use
+ * spmm_plan_reserve beforehand to keep allocation out of timed or captured
+ * regions).
+ * (ParamSpMM section 2, Algorithm 1; graph-spmm model card, "Method".)
+ */
+spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, const float *B,
+                     int64_t N, spmm_reduce reduce, float *C, int32_t *argmax, void *stream);
+
+/*
+ * spmm_plan_reserve -- allocate the workspace spmm_run needs for (N, reduce)
+ * now. Synchronous (cudaMalloc). Returns SPMM_ERR_OOM on failure.
+ */
+spmm_status spmm_plan_reserve(spmm_plan_t plan, int64_t N, spmm_reduce reduce);
+
+/*
+ * spmm_plan_validate_cols -- check that every col[p], p < nnz, lies in [0, K).
+ *   col : device, int32 [nnz]. Synchronous on `stream`.
+ * Returns SPMM_ERR_INVALID_INPUT if any entry is out of range.
+ */
+spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *stream);
+
+/*
+ * spmm_plan_sync -- wait for `stream`, then report any error a kernel of this
+ * plan recorded on the device (SPMM_ERR_TIMEOUT when a bounded wait gave up)
+ * and clear it. Synchronous.
+ */
+spmm_status spmm_plan_sync(spmm_plan_t plan, void *stream);
+
+/*
+ * spmm_plan_describe -- descriptors plus the routing decision spmm_run will
+ * take for (N, reduce) with 16-byte aligned B and C. Host only, no CUDA call.
+ */
+spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce,
+                               spmm_plan_info *out);
+
+/*
+ * spmm_plan_set_family -- pin the light-row family (SPMM_FAMILY_AUTO restores
+ * the router) and the heavy-row threshold (t_split <= 0 restores the default;
+ * a new threshold rebuilds the heavy-row tables, synchronously on the legacy
+ * default stream). For tests and benchmarks of individual families.
+ */
+spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split);
+
+/*
+ * spmm_route -- the router as a pure host function. Reads the descriptor
+ * fields of *desc (M, K, nnz, d_max, dbar, cv, t_split, chunk, n_heavy,
+ * n_chunks) and fills the launch-shape fields of *out for (N, reduce) on a GPU
+ * with `num_sms` SMs; `aligned` says whether B and C are 16-byte aligned.
+ * No CUDA call. (RA-SpMM "routing rules": first matching rule wins.)
+ */
+spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce, int aligned,
+                       int num_sms, int family_override, spmm_plan_info *out);
+
+/*
+ * spmm_default_t_split -- the heavy-row threshold the plan uses for a graph of
+ * `nnz` entries on `num_sms` SMs (pure host function).
+ */
+int64_t spmm_default_t_split(int64_t M, int64_t nnz, int num_sms);
+
+/* spmm_plan_destroy -- free the plan and everything it owns. NULL is a no-op. */
+spmm_status spmm_plan_destroy(spmm_plan_t plan);
+
+/* spmm_status_string -- static description of a status code. */
+const char *spmm_status_string(spmm_status status);
+
+/* spmm_launch_count -- kernels this library has launched in this process. */
+uint64_t spmm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_SPMM_H */

@@ -1,0 +1,191 @@
+// Shared definitions of the CUDA library: the plan, the per-launch argument
+// block, load/store helpers with cache hints, and the reduction operators.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <atomic>
+#include <climits>
+
+#include "spmm.h"
+
+namespace spmm {
+
+constexpr int kWarp = 32;
+constexpr int kMaxTilesY = 65535;
+
+// Everything a plan owns. Host-side object; the pointers are device memory.
+struct Plan {
+    int device = 0;
+    int num_sms = 0;
+    int64_t M = 0, K = 0, nnz = 0;
+    int64_t d_max = 0, n_empty = 0;
+    double dbar = 0.0, cv = 0.0;
+
+    int32_t *rowptr = nullptr;       // plan copy of rowptr [M+1]
+
+    // heavy rows (d > t_split): ids ascending, chunk table (row, begin) per
+    // chunk of `chunk` entries, first chunk of each heavy row (prefix, n_heavy+1)
+    int64_t t_split = 0, t_split_default = 0;
+    int64_t chunk = 0;
+    int64_t n_heavy = 0, n_chunks = 0;
+    int32_t *heavy_rows = nullptr;
+    int32_t *heavy_chunk0 = nullptr;
+    int2 *chunks = nullptr;
+
+    // workspace for chunk partials: [n_chunks][N] fp32 (+ int32 for max)
+    void *work = nullptr;
+    size_t work_bytes = 0;
+
+    int32_t *err = nullptr;          // device error words, see kErr*
+    int family_override = SPMM_FAMILY_AUTO;
+};
+
+enum { kErrTimeout = 0, kErrBadCol = 1, kErrWords = 4 };
+
+// Arguments of one spmm_run launch (passed by value to the kernels).
+struct RunArgs {
+    const int32_t *__restrict__ rowptr;
+    const int32_t *__restrict__ col;
+    const float *__restrict__ val;
+    const float *__restrict__ B;
+    float *__restrict__ C;
+    int32_t *__restrict__ argmax;
+    int64_t M;
+    int32_t N;          // feature width (columns of B and C)
+    int32_t n_vec;      // N / vec
+    int32_t t_split;    // light kernels skip rows with more entries than this
+    int32_t chunk;      // entries per heavy-row chunk
+    int32_t n_chunks, n_heavy;
+    const int2 *__restrict__ chunks;          // (row, begin) per chunk
+    const int32_t *__restrict__ heavy_rows;   // [n_heavy]
+    const int32_t *__restrict__ heavy_chunk0; // [n_heavy + 1]
+    float *__restrict__ ws_val;               // [n_chunks][N]
+    int32_t *__restrict__ ws_arg;             // [n_chunks][N] (max only)
+    int32_t *__restrict__ err;
+};
+
+// --- global loads / stores with cache hints --------------------------------
+// Gathered B rows are re-read by other rows: keep them in L1/L2 (ld.global.nc).
+// col / val / rowptr are streamed once: evict-first. C is written once: streaming store.
+
+__device__ __forceinline__ int ld_stream(const int32_t *p) { return __ldcs(p); }
+__device__ __forceinline__ float ld_stream(const float *p) { return __ldcs(p); }
+
+template <int V> struct VecT;
+template <> struct VecT<1> { using type = float; };
+template <> struct VecT<4> { using type = float4; };
+
+template <int V>
+__device__ __forceinline__ void ld_vec(const float *p, float (&x)[V]) {
+    if constexpr (V == 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(p));
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+        x[0] = __ldg(p);
+    }
+}
+
+template <int V>
+__device__ __forceinline__ void st_vec(float *p, const float (&x)[V]) {
+    if constexpr (V == 4) {
+        __stcs(reinterpret_cast<float4 *>(p), make_float4(x[0], x[1], x[2], x[3]));
+    } else {
+        __stcs(p, x[0]);
+    }
+}
+
+template <int V>
+__device__ __forceinline__ void st_vec_i(int32_t *p, const int (&x)[V]) {
+    if constexpr (V == 4) {
+        __stcs(reinterpret_cast<int4 *>(p), make_int4(x[0], x[1], x[2], x[3]));
+    } else {
+        __stcs(p, x[0]);
+    }
+}
+
+// --- reductions -------------------------------------------------------------
+// sum / mean: fp32 fused multiply-add per entry; the order is fixed by the
+// kernel's mapping. max: (value, column) with the total order "larger value,
+// then smaller column"; the identity (-inf, INT_MAX) marks "no entry yet".
+
+constexpr int kNoCol = INT_MAX;
+
+__device__ __forceinline__ bool max_better(float y, int jy, float v, int jv) {
+    return y > v || (y == v && jy < jv);
+}
+
+template <int V, int RED, bool HAS_VAL>
+struct Acc {
+    float v[V];
+    int j[V];   // used by max only
+
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            v[e] = (RED == SPMM_MAX) ? -__int_as_float(0x7f800000) : 0.0f;
+            j[e] = kNoCol;
+        }
+    }
+
+    __device__ __forceinline__ void add(float a, int col, const float (&b)[V]) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            if constexpr (RED == SPMM_MAX) {
+                const float y = HAS_VAL ? __fmul_rn(a, b[e]) : b[e];
+                if (max_better(y, col, v[e], j[e])) { v[e] = y; j[e] = col; }
+            } else {
+                v[e] = HAS_VAL ? __fmaf_rn(a, b[e], v[e]) : __fadd_rn(v[e], b[e]);
+            }
+        }
+    }
+
+    // combine with the accumulator held by lane (lane ^ offset)
+    __device__ __forceinline__ void combine_xor(int offset) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v[e], offset);
+            if constexpr (RED == SPMM_MAX) {
+                const int oj = __shfl_xor_sync(0xffffffffu, j[e], offset);
+                if (max_better(ov, oj, v[e], j[e])) { v[e] = ov; j[e] = oj; }
+            } else {
+                // both partners compute the same sum (a + b == b + a bit for bit)
+                v[e] = __fadd_rn(v[e], ov);
+            }
+        }
+    }
+
+    // final values for a row of d stored entries
+    __device__ __forceinline__ void finish(int d, float (&out)[V], int (&arg)[V]) const {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            if constexpr (RED == SPMM_MAX) {
+                const bool none = (j[e] == kNoCol);
+                out[e] = none ? 0.0f : v[e];
+                arg[e] = none ? -1 : j[e];
+            } else if constexpr (RED == SPMM_MEAN) {
+                out[e] = d > 0 ? __fdiv_rn(v[e], (float)d) : 0.0f;
+                arg[e] = 0;
+            } else {
+                out[e] = v[e];
+                arg[e] = 0;
+            }
+        }
+    }
+};
+
+// Number of kernels launched by this library (spmm_launch_count).
+extern std::atomic<uint64_t> g_launches;
+inline void count_launch(uint64_t n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// Family launchers (one translation unit each). Return a CUDA error code.
+cudaError_t launch_rowgroup(const RunArgs &a, int vec, int lanes, int reduce, bool has_val,
+                            int tiles, cudaStream_t s);
+cudaError_t launch_warprow(const RunArgs &a, int vec, int lanes, int reduce, bool has_val,
+                           int tiles, cudaStream_t s);
+cudaError_t launch_heavy(const RunArgs &a, int vec, int lanes, int reduce, bool has_val,
+                         int tiles, cudaStream_t s);
+
+}  // namespace spmm

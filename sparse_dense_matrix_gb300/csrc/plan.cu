@@ -1,0 +1,554 @@
+// The C ABI: plan creation (descriptors, heavy-row tables), the router,
+// spmm_run's dispatch, validation and status reporting.
+//
+// Plan creation is one O(M) pass over rowptr on the device (RA-SpMM abstract
+// and "routing rules": M, mean degree d = nnz/M and the degree coefficient of
+// variation CV_d from the row-pointer array alone), plus an ordered compaction
+// of the heavy rows. Integer sums are exact (64-bit), so the descriptors and
+// every routing decision are deterministic.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <cmath>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+
+namespace spmm {
+
+std::atomic<uint64_t> g_launches{0};
+
+namespace {
+
+constexpr int kDescThreads = 256;
+constexpr int kDescRowsPerBlock = 4096;
+
+struct BlockStats {
+    unsigned long long s1, s2;   // sum of degrees, sum of squared degrees
+    int dmax, n_empty, n_bad, n_heavy;
+};
+
+// ---------------------------------------------------------------- allocation
+// Host-side fault injection for the tests: SPMM_FAULT_ALLOC=n makes the n-th
+// device allocation of a spmm_plan_create call fail (as if the device were full).
+thread_local int t_alloc_countdown = 0;
+
+cudaError_t dev_alloc(void **p, size_t bytes) {
+    *p = nullptr;
+    if (t_alloc_countdown > 0 && --t_alloc_countdown == 0) return cudaErrorMemoryAllocation;
+    if (bytes == 0) bytes = 16;
+    return cudaMalloc(p, bytes);
+}
+
+void dev_free(void *p) {
+    if (p) cudaFree(p);
+}
+
+spmm_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return SPMM_OK;
+    if (e == cudaErrorMemoryAllocation) return SPMM_ERR_OOM;
+    return SPMM_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ device kernels
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+__device__ __forceinline__ int warp_sum_i(int x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+__device__ __forceinline__ int warp_max_i(int x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+// Block b summarises rows [b*R, (b+1)*R): degree sums, max, empty rows,
+// decreasing row pointers, rows above t_split.
+__global__ void __launch_bounds__(kDescThreads) k_desc(const int32_t *__restrict__ rowptr,
+                                                      int64_t M, int64_t t_split,
+                                                      BlockStats *__restrict__ out) {
+    const int64_t r0 = (int64_t)blockIdx.x * kDescRowsPerBlock;
+    const int64_t r1 = min(M, r0 + kDescRowsPerBlock);
+    unsigned long long s1 = 0, s2 = 0;
+    int dmax = 0, n_empty = 0, n_bad = 0, n_heavy = 0;
+    for (int64_t r = r0 + threadIdx.x; r < r1; r += kDescThreads) {
+        const int d = rowptr[r + 1] - rowptr[r];
+        if (d < 0) { ++n_bad; continue; }
+        s1 += (unsigned long long)d;
+        s2 += (unsigned long long)d * (unsigned long long)d;
+        dmax = max(dmax, d);
+        n_empty += (d == 0);
+        n_heavy += (d > t_split);
+    }
+    s1 = warp_sum_u64(s1);
+    s2 = warp_sum_u64(s2);
+    dmax = warp_max_i(dmax);
+    n_empty = warp_sum_i(n_empty);
+    n_bad = warp_sum_i(n_bad);
+    n_heavy = warp_sum_i(n_heavy);
+    __shared__ BlockStats sh[kDescThreads / kWarp];
+    const int w = threadIdx.x / kWarp;
+    if ((threadIdx.x & 31) == 0) sh[w] = BlockStats{s1, s2, dmax, n_empty, n_bad, n_heavy};
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        BlockStats t = sh[0];
+        for (int i = 1; i < kDescThreads / kWarp; ++i) {
+            t.s1 += sh[i].s1;
+            t.s2 += sh[i].s2;
+            t.dmax = max(t.dmax, sh[i].dmax);
+            t.n_empty += sh[i].n_empty;
+            t.n_bad += sh[i].n_bad;
+            t.n_heavy += sh[i].n_heavy;
+        }
+        out[blockIdx.x] = t;
+    }
+}
+
+// Ordered compaction of the heavy rows of block b's row range to offset[b]:
+// rows are taken in rounds of kDescThreads consecutive rows, ranked by warp
+// ballots and a scan over the warps.
+__global__ void __launch_bounds__(kDescThreads) k_heavy_list(const int32_t *__restrict__ rowptr,
+                                                            int64_t M, int64_t t_split,
+                                                            const int32_t *__restrict__ offset,
+                                                            int32_t *__restrict__ heavy_rows,
+                                                            int2 *__restrict__ heavy_span) {
+    constexpr int kWarps = kDescThreads / kWarp;
+    __shared__ int warp_count[kWarps];
+    const int64_t r0 = (int64_t)blockIdx.x * kDescRowsPerBlock;
+    const int64_t r1 = min(M, r0 + kDescRowsPerBlock);
+    const int lane = threadIdx.x & 31, w = threadIdx.x / kWarp;
+    int base = offset[blockIdx.x];
+    for (int64_t rb = r0; rb < r1; rb += kDescThreads) {
+        const int64_t r = rb + threadIdx.x;
+        int b = 0, e = 0;
+        bool heavy = false;
+        if (r < r1) {
+            b = rowptr[r];
+            e = rowptr[r + 1];
+            heavy = (e - b) > t_split;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, heavy);
+        if (lane == 0) warp_count[w] = __popc(m);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int i = 0; i < kWarps; ++i) {
+            before += (i < w) ? warp_count[i] : 0;
+            total += warp_count[i];
+        }
+        if (heavy) {
+            const int pos = base + before + __popc(m & ((1u << lane) - 1u));
+            heavy_rows[pos] = (int)r;
+            heavy_span[pos] = make_int2(b, e);
+        }
+        base += total;
+        __syncthreads();
+    }
+}
+
+__global__ void k_check_cols(const int32_t *__restrict__ col, int64_t nnz, int64_t K,
+                             int32_t *__restrict__ err) {
+    int bad = 0;
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < nnz;
+         p += (int64_t)gridDim.x * blockDim.x) {
+        const int c = col[p];
+        bad |= (c < 0 || (int64_t)c >= K);
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err + kErrBadCol, 1);
+}
+
+// ------------------------------------------------------------- host helpers
+int64_t pow2ceil(int64_t x) {
+    int64_t p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+void free_heavy(Plan *p) {
+    dev_free(p->heavy_rows);
+    dev_free(p->heavy_chunk0);
+    dev_free(p->chunks);
+    p->heavy_rows = nullptr;
+    p->heavy_chunk0 = nullptr;
+    p->chunks = nullptr;
+    p->n_heavy = p->n_chunks = 0;
+}
+
+// Descriptors, validation and heavy-row tables for threshold t_split.
+spmm_status analyse(Plan *p, int64_t t_split, cudaStream_t s) {
+    free_heavy(p);
+    p->t_split = t_split;
+    p->chunk = std::max<int64_t>(32, t_split / 2);
+    if (p->M == 0) return SPMM_OK;
+    const int64_t nblk = (p->M + kDescRowsPerBlock - 1) / kDescRowsPerBlock;
+    BlockStats *d_stats = nullptr;
+    int32_t *d_off = nullptr;
+    int2 *d_span = nullptr;
+    spmm_status st = SPMM_OK;
+    std::vector<BlockStats> hs(nblk);
+    std::vector<int32_t> off(nblk + 1, 0);
+    cudaError_t e = dev_alloc((void **)&d_stats, sizeof(BlockStats) * nblk);
+    if (e != cudaSuccess) return from_cuda(e);
+    k_desc<<<(unsigned)nblk, kDescThreads, 0, s>>>(p->rowptr, p->M, t_split, d_stats);
+    count_launch();
+    e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(hs.data(), d_stats, sizeof(BlockStats) * nblk, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) { st = from_cuda(e); goto done; }
+    {
+        unsigned long long s1 = 0, s2 = 0;
+        int64_t dmax = 0, empty = 0, bad = 0, heavy = 0;
+        for (int64_t b = 0; b < nblk; ++b) {
+            s1 += hs[b].s1;
+            s2 += hs[b].s2;
+            dmax = std::max<int64_t>(dmax, hs[b].dmax);
+            empty += hs[b].n_empty;
+            bad += hs[b].n_bad;
+            off[b] = (int32_t)heavy;
+            heavy += hs[b].n_heavy;
+        }
+        off[nblk] = (int32_t)heavy;
+        if (bad || (int64_t)s1 != p->nnz) { st = SPMM_ERR_INVALID_INPUT; goto done; }
+        p->d_max = dmax;
+        p->n_empty = empty;
+        p->dbar = (double)s1 / (double)p->M;
+        const double var = (double)s2 / (double)p->M - p->dbar * p->dbar;
+        p->cv = s1 == 0 ? 0.0 : std::sqrt(var > 0.0 ? var : 0.0) / p->dbar;
+        p->n_heavy = heavy;
+    }
+    if (p->n_heavy > 0) {
+        const int64_t nh = p->n_heavy;
+        e = dev_alloc((void **)&d_off, sizeof(int32_t) * (nblk + 1));
+        if (e == cudaSuccess) e = dev_alloc((void **)&p->heavy_rows, sizeof(int32_t) * nh);
+        if (e == cudaSuccess) e = dev_alloc((void **)&d_span, sizeof(int2) * nh);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(d_off, off.data(), sizeof(int32_t) * (nblk + 1), cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) {
+            k_heavy_list<<<(unsigned)nblk, kDescThreads, 0, s>>>(p->rowptr, p->M, t_split, d_off,
+                                                                 p->heavy_rows, d_span);
+            count_launch();
+            e = cudaGetLastError();
+        }
+        std::vector<int2> span(nh);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(span.data(), d_span, sizeof(int2) * nh, cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) { st = from_cuda(e); goto done; }
+        // chunk table: heavy row h is cut into ceil(d_h / chunk) chunks
+        std::vector<int32_t> c0(nh + 1, 0);
+        std::vector<int2> chunks;
+        std::vector<int32_t> rows(nh);
+        e = cudaMemcpy(rows.data(), p->heavy_rows, sizeof(int32_t) * nh, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) { st = from_cuda(e); goto done; }
+        for (int64_t h = 0; h < nh; ++h) {
+            c0[h] = (int32_t)chunks.size();
+            for (int64_t q = span[h].x; q < span[h].y; q += p->chunk)
+                chunks.push_back(make_int2(rows[h], (int)q));
+        }
+        c0[nh] = (int32_t)chunks.size();
+        p->n_chunks = (int64_t)chunks.size();
+        e = dev_alloc((void **)&p->heavy_chunk0, sizeof(int32_t) * (nh + 1));
+        if (e == cudaSuccess) e = dev_alloc((void **)&p->chunks, sizeof(int2) * p->n_chunks);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(p->heavy_chunk0, c0.data(), sizeof(int32_t) * (nh + 1), cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(p->chunks, chunks.data(), sizeof(int2) * p->n_chunks, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) { st = from_cuda(e); goto done; }
+    }
+done:
+    dev_free(d_stats);
+    dev_free(d_off);
+    dev_free(d_span);
+    if (st != SPMM_OK) free_heavy(p);
+    return st;
+}
+
+void destroy(Plan *p) {
+    if (!p) return;
+    free_heavy(p);
+    dev_free(p->rowptr);
+    dev_free(p->work);
+    dev_free(p->err);
+    delete p;
+}
+
+size_t workspace_need(const Plan *p, int64_t N, int reduce) {
+    if (p->n_heavy == 0 || N == 0) return 0;
+    const size_t per = (size_t)p->n_chunks * (size_t)N * 4;
+    return reduce == SPMM_MAX ? 2 * per : per;
+}
+
+spmm_status ensure_workspace(Plan *p, size_t need) {
+    if (need <= p->work_bytes) return SPMM_OK;
+    dev_free(p->work);
+    p->work = nullptr;
+    p->work_bytes = 0;
+    void *w = nullptr;
+    cudaError_t e = cudaMalloc(&w, need);
+    if (e != cudaSuccess) return from_cuda(e);
+    p->work = w;
+    p->work_bytes = need;
+    return SPMM_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ router
+// Rules, first match wins (RA-SpMM "routing rules": descriptors + N -> family):
+//   R0  a family pinned by spmm_plan_set_family is used as given;
+//   R1  wide N (more than 32 column vectors per row)      -> WARPROW with column tiles;
+//   R2  near-uniform degrees (CV_d <= 1) and narrow N      -> ROWGROUP, 32/L rows per warp;
+//   R3  otherwise (skewed degrees)                          -> WARPROW.
+// Independently of the family, rows with more than t_split entries are split
+// into chunks (two extra launches) whenever the plan holds such rows.
+static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int aligned, int num_sms,
+                       int family_override, spmm_plan_info *o) {
+    if (o != d) *o = *d;
+    o->N = N;
+    o->reduce = reduce;
+    o->num_sms = num_sms;
+    o->vec = (aligned && N % 4 == 0) ? 4 : 1;
+    const int64_t n_vec = (N + o->vec - 1) / o->vec;
+    const int64_t lanes = std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil(n_vec)));
+    o->lanes = (int32_t)lanes;
+    o->col_tiles = (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
+    int fam;
+    if (family_override != SPMM_FAMILY_AUTO)
+        fam = family_override == SPMM_FAMILY_COLTILE ? SPMM_FAMILY_WARPROW : family_override;
+    else if (n_vec > 32)
+        fam = SPMM_FAMILY_WARPROW;
+    else if (d->cv <= 1.0)
+        fam = SPMM_FAMILY_ROWGROUP;
+    else
+        fam = SPMM_FAMILY_WARPROW;
+    o->family = fam;
+    o->rows_per_warp = fam == SPMM_FAMILY_ROWGROUP ? (int32_t)(32 / lanes) : 1;
+    o->launches = (d->M > 0 && N > 0) ? 1 + (d->n_heavy > 0 ? 2 : 0) : 0;
+    const size_t per = (size_t)d->n_chunks * (size_t)N * 4;
+    o->workspace_bytes = d->n_heavy > 0 ? (int64_t)(reduce == SPMM_MAX ? 2 * per : per) : 0;
+}
+
+}  // namespace spmm
+
+using namespace spmm;
+
+extern "C" {
+
+int64_t spmm_default_t_split(int64_t M, int64_t nnz, int num_sms) {
+    (void)M;
+    // A row holding more than ~1/128 of one SM's share of the entries would
+    // run for a large fraction of the launch on a single warp: split it.
+    const int64_t sms = num_sms > 0 ? num_sms : 1;
+    const int64_t share = nnz / (128 * sms);
+    return std::max<int64_t>(256, share);
+}
+
+spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce, int aligned,
+                       int num_sms, int family_override, spmm_plan_info *out) {
+    if (!desc || !out || N < 0) return SPMM_ERR_INVALID_ARG;
+    if (reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
+    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_COLTILE)
+        return SPMM_ERR_INVALID_ARG;
+    route_fill(desc, N, reduce, aligned, num_sms, family_override, out);
+    return SPMM_OK;
+}
+
+const char *spmm_status_string(spmm_status s) {
+    switch (s) {
+        case SPMM_OK: return "ok";
+        case SPMM_ERR_INVALID_ARG: return "invalid argument";
+        case SPMM_ERR_INVALID_INPUT: return "invalid input (rowptr not a CSR row-pointer array, or a column out of range)";
+        case SPMM_ERR_OOM: return "out of memory";
+        case SPMM_ERR_CUDA: return "CUDA runtime error";
+        case SPMM_ERR_UNSUPPORTED: return "unsupported size";
+        case SPMM_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    }
+    return "unknown status";
+}
+
+uint64_t spmm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *stream,
+                             spmm_plan_t *out) {
+    if (!out) return SPMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (M < 0 || K < 0 || !rowptr) return SPMM_ERR_INVALID_ARG;
+    if (M >= INT32_MAX || K >= INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+    const char *fault = std::getenv("SPMM_FAULT_ALLOC");
+    t_alloc_countdown = fault ? std::atoi(fault) : 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    Plan *p = new (std::nothrow) Plan();
+    if (!p) return SPMM_ERR_OOM;
+    p->M = M;
+    p->K = K;
+    spmm_status st = SPMM_OK;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e == cudaSuccess) e = dev_alloc((void **)&p->rowptr, sizeof(int32_t) * (M + 1));
+    if (e == cudaSuccess) e = dev_alloc((void **)&p->err, sizeof(int32_t) * kErrWords);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->err, 0, sizeof(int32_t) * kErrWords, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(p->rowptr, rowptr, sizeof(int32_t) * (M + 1), cudaMemcpyDefault, s);
+    int32_t ends[2] = {0, 0};
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&ends[0], p->rowptr, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&ends[1], p->rowptr + M, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        st = from_cuda(e);
+    } else if (ends[0] != 0 || ends[1] < 0) {
+        st = SPMM_ERR_INVALID_INPUT;
+    } else {
+        p->nnz = ends[1];
+        p->t_split_default = spmm_default_t_split(M, p->nnz, p->num_sms);
+        st = analyse(p, p->t_split_default, s);
+    }
+    t_alloc_countdown = 0;
+    if (st != SPMM_OK) {
+        destroy(p);
+        return st;
+    }
+    *out = reinterpret_cast<spmm_plan_t>(p);
+    return SPMM_OK;
+}
+
+spmm_status spmm_plan_destroy(spmm_plan_t plan) {
+    destroy(reinterpret_cast<Plan *>(plan));
+    return SPMM_OK;
+}
+
+static void fill_desc(const Plan *p, spmm_plan_info *o) {
+    std::memset(o, 0, sizeof(*o));
+    o->M = p->M;
+    o->K = p->K;
+    o->nnz = p->nnz;
+    o->d_max = p->d_max;
+    o->n_empty = p->n_empty;
+    o->dbar = p->dbar;
+    o->cv = p->cv;
+    o->t_split = p->t_split;
+    o->chunk = p->chunk;
+    o->n_heavy = p->n_heavy;
+    o->n_chunks = p->n_chunks;
+}
+
+spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce, spmm_plan_info *out) {
+    if (!plan || !out || N < 0 || reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
+    const Plan *p = reinterpret_cast<const Plan *>(plan);
+    fill_desc(p, out);
+    route_fill(out, N, reduce, 1, p->num_sms, p->family_override, out);
+    return SPMM_OK;
+}
+
+spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split) {
+    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_COLTILE) return SPMM_ERR_INVALID_ARG;
+    Plan *p = reinterpret_cast<Plan *>(plan);
+    p->family_override = family;
+    const int64_t want = t_split > 0 ? t_split : p->t_split_default;
+    if (want == p->t_split) return SPMM_OK;
+    cudaError_t e = cudaDeviceSynchronize();   // the workspace and tables may be in use
+    if (e != cudaSuccess) return from_cuda(e);
+    return analyse(p, want, nullptr);
+}
+
+spmm_status spmm_plan_reserve(spmm_plan_t plan, int64_t N, spmm_reduce reduce) {
+    if (!plan || N < 0 || reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
+    Plan *p = reinterpret_cast<Plan *>(plan);
+    return ensure_workspace(p, workspace_need(p, N, reduce));
+}
+
+spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *stream) {
+    if (!plan) return SPMM_ERR_INVALID_ARG;
+    Plan *p = reinterpret_cast<Plan *>(plan);
+    if (p->nnz == 0) return SPMM_OK;
+    if (!col) return SPMM_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t flag = 0;
+    cudaError_t e = cudaMemsetAsync(p->err + kErrBadCol, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) {
+        const int64_t blocks = std::min<int64_t>((p->nnz + 255) / 256, (int64_t)p->num_sms * 8);
+        k_check_cols<<<(unsigned)blocks, 256, 0, s>>>(col, p->nnz, p->K, p->err);
+        count_launch();
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&flag, p->err + kErrBadCol, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return flag ? SPMM_ERR_INVALID_INPUT : SPMM_OK;
+}
+
+spmm_status spmm_plan_sync(spmm_plan_t plan, void *stream) {
+    if (!plan) return SPMM_ERR_INVALID_ARG;
+    Plan *p = reinterpret_cast<Plan *>(plan);
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t words[kErrWords] = {0};
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpy(words, p->err, sizeof(words), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(p->err, 0, sizeof(words));
+    if (e != cudaSuccess) return from_cuda(e);
+    if (words[kErrTimeout]) return SPMM_ERR_TIMEOUT;
+    return SPMM_OK;
+}
+
+spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, const float *B,
+                     int64_t N, spmm_reduce reduce, float *C, int32_t *argmax, void *stream) {
+    if (!plan || N < 0 || reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
+    Plan *p = reinterpret_cast<Plan *>(plan);
+    if (p->M == 0 || N == 0) return SPMM_OK;
+    if (!C) return SPMM_ERR_INVALID_ARG;
+    if (p->nnz > 0 && (!col || !B)) return SPMM_ERR_INVALID_ARG;
+    if (N >= INT32_MAX / 4) return SPMM_ERR_UNSUPPORTED;
+    if (reduce != SPMM_MAX) argmax = nullptr;
+    const int aligned = ((uintptr_t)B % 16 == 0) && ((uintptr_t)C % 16 == 0) &&
+                        ((uintptr_t)argmax % 16 == 0);
+    spmm_plan_info r;
+    fill_desc(p, &r);
+    route_fill(&r, N, reduce, aligned, p->num_sms, p->family_override, &r);
+    if (r.col_tiles > kMaxTilesY) return SPMM_ERR_UNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+
+    RunArgs a{};
+    a.rowptr = p->rowptr;
+    a.col = col;
+    a.val = val;
+    a.B = B;
+    a.C = C;
+    a.argmax = argmax;
+    a.M = p->M;
+    a.N = (int32_t)N;
+    a.n_vec = (int32_t)((N + r.vec - 1) / r.vec);
+    a.t_split = (int32_t)p->t_split;
+    a.chunk = (int32_t)p->chunk;
+    a.n_chunks = (int32_t)p->n_chunks;
+    a.n_heavy = (int32_t)p->n_heavy;
+    a.chunks = p->chunks;
+    a.heavy_rows = p->heavy_rows;
+    a.heavy_chunk0 = p->heavy_chunk0;
+    a.err = p->err;
+    if (p->n_heavy > 0) {
+        spmm_status st = ensure_workspace(p, workspace_need(p, N, reduce));
+        if (st != SPMM_OK) return st;
+        a.ws_val = reinterpret_cast<float *>(p->work);
+        a.ws_arg = reduce == SPMM_MAX
+                       ? reinterpret_cast<int32_t *>(reinterpret_cast<char *>(p->work) +
+                                                     (size_t)p->n_chunks * (size_t)N * 4)
+                       : nullptr;
+    }
+    const bool has_val = val != nullptr;
+    cudaError_t e;
+    if (r.family == SPMM_FAMILY_ROWGROUP)
+        e = launch_rowgroup(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
+    else
+        e = launch_warprow(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
+    if (e == cudaSuccess && p->n_heavy > 0)
+        e = launch_heavy(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
+    return from_cuda(e);
+}
+
+}  // extern "C"

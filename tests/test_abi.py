@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+rejects bad arguments on the host, and its router is a pure function."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sdm():
+    from sparse_dense_matrix_gb300 import _build
+    _build.build()
+    import sparse_dense_matrix_gb300 as m
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "spmm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spmm_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("spmm_plan_create", "spmm_run", "spmm_plan_describe", "spmm_plan_destroy",
+                 "spmm_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(sdm):
+    lib = ctypes.CDLL(os.path.join(ROOT, "sparse_dense_matrix_gb300", "libspmm.so"))
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(sdm):
+    for code in range(7):
+        assert sdm.spmm_status_string(code)
+    assert sdm.spmm_status_string(0) == "ok"
+    assert "unknown" in sdm.spmm_status_string(99)
+
+
+def test_host_argument_checks(sdm):
+    lib = sdm.lib
+    out = ctypes.c_void_p(123)
+    assert lib.spmm_plan_create(None, 10, 10, None, ctypes.byref(out)) == 1
+    assert out.value is None                      # cleared on error
+    assert lib.spmm_plan_create(ctypes.c_void_p(16), -1, 10, None, ctypes.byref(out)) == 1
+    assert lib.spmm_plan_create(ctypes.c_void_p(16), 10, 10, None, None) == 1
+    assert lib.spmm_plan_create(ctypes.c_void_p(16), 1 << 31, 10, None, ctypes.byref(out)) == 5
+    assert lib.spmm_run(None, None, None, None, 4, 0, None, None, None) == 1
+    assert lib.spmm_plan_reserve(None, 4, 0) == 1
+    assert lib.spmm_plan_validate_cols(None, None, None) == 1
+    assert lib.spmm_plan_sync(None, None) == 1
+    info = sdm.PlanInfo()
+    assert lib.spmm_plan_describe(None, 4, 0, ctypes.byref(info)) == 1
+    assert lib.spmm_plan_set_family(None, 0, 0) == 1
+    assert lib.spmm_plan_destroy(None) == 0
+    assert lib.spmm_route(ctypes.byref(info), 4, 7, 1, 152, -1, ctypes.byref(info)) == 1
+    assert lib.spmm_route(ctypes.byref(info), -4, 0, 1, 152, -1, ctypes.byref(info)) == 1
+    assert lib.spmm_route(ctypes.byref(info), 4, 0, 1, 152, 9, ctypes.byref(info)) == 1
+
+
+def test_plan_create_without_a_gpu_reports_cuda_error(sdm):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("only meaningful on a host without a GPU")
+    out = ctypes.c_void_p()
+    # never dereferenced: the device query fails first
+    assert sdm.lib.spmm_plan_create(ctypes.c_void_p(4096), 10, 10, None, ctypes.byref(out)) == 4
+
+
+def _desc(M=1 << 20, nnz=10 << 20, cv=0.0, n_heavy=0, n_chunks=0, t_split=512):
+    return dict(M=M, K=M, nnz=nnz, dbar=nnz / M, cv=cv, d_max=10, n_empty=0,
+                t_split=t_split, chunk=t_split // 2, n_heavy=n_heavy, n_chunks=n_chunks)
+
+
+def test_router_rules(sdm):
+    r = sdm.spmm_route(_desc(cv=0.0), 16, 0)
+    assert (r["family_name"], r["vec"], r["lanes"], r["rows_per_warp"], r["col_tiles"]) == \
+        ("rowgroup", 4, 4, 8, 1)
+    r = sdm.spmm_route(_desc(cv=0.0), 64, 1)
+    assert (r["family_name"], r["lanes"], r["rows_per_warp"]) == ("rowgroup", 16, 2)
+    r = sdm.spmm_route(_desc(cv=9.2), 64, 0)
+    assert (r["family_name"], r["lanes"], r["rows_per_warp"]) == ("warprow", 16, 1)
+    r = sdm.spmm_route(_desc(cv=0.1), 512, 0)                 # wide N: column tiles
+    assert (r["family_name"], r["vec"], r["lanes"], r["col_tiles"]) == ("warprow", 4, 32, 4)
+    r = sdm.spmm_route(_desc(cv=0.0), 16, 0, aligned=False)    # scalar path
+    assert (r["vec"], r["lanes"], r["rows_per_warp"]) == (1, 16, 2)
+    r = sdm.spmm_route(_desc(cv=0.0), 17, 0)                   # N % 4 != 0
+    assert (r["vec"], r["lanes"], r["col_tiles"]) == (1, 32, 1)
+    r = sdm.spmm_route(_desc(cv=0.0), 33, 0)
+    assert (r["family_name"], r["vec"], r["col_tiles"]) == ("warprow", 1, 2)
+    r = sdm.spmm_route(_desc(cv=0.0), 1, 2)
+    assert (r["vec"], r["lanes"], r["rows_per_warp"]) == (1, 2, 16)
+    r = sdm.spmm_route(_desc(cv=0.0), 16, 0, family=sdm.FAMILY["warprow"])
+    assert r["family_name"] == "warprow"
+
+
+def test_router_split_launches_and_workspace(sdm):
+    r = sdm.spmm_route(_desc(cv=9.0, n_heavy=3, n_chunks=40), 64, 0)
+    assert r["launches"] == 3 and r["workspace_bytes"] == 40 * 64 * 4
+    r = sdm.spmm_route(_desc(cv=9.0, n_heavy=3, n_chunks=40), 64, 2)
+    assert r["workspace_bytes"] == 2 * 40 * 64 * 4             # values + argmax partials
+    r = sdm.spmm_route(_desc(), 64, 0)
+    assert r["launches"] == 1 and r["workspace_bytes"] == 0
+    r = sdm.spmm_route(_desc(), 0, 0)
+    assert r["launches"] == 0
+
+
+def test_default_split_threshold(sdm):
+    assert sdm.spmm_default_t_split(2048, 16384, 152) == 256
+    assert sdm.spmm_default_t_split(1 << 22, 104_839_949, 152) == 104_839_949 // (128 * 152)
+    assert sdm.spmm_default_t_split(10, 10, 0) == 256
+
+
+def test_tensor_api_refuses_cpu_tensors(sdm):
+    torch = pytest.importorskip("torch")
+    rp = torch.zeros(3, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        sdm.SparseAdj(rp, torch.zeros(0, dtype=torch.int32))
