@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def sdm():
-    from sparse_dense_matrix_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import sparse_dense_matrix_gb300 as m
     return m
 
