@@ -55,8 +55,11 @@ typedef enum {
     SPMM_FAMILY_AUTO = -1,     /* let the router decide                                  */
     SPMM_FAMILY_ROWGROUP = 0,  /* several rows per warp, L lanes per row (uniform degree) */
     SPMM_FAMILY_WARPROW = 1,   /* one warp per row, lane groups split the row's entries   */
-    SPMM_FAMILY_COLTILE = 2    /* a CTA per row block, warps own 128-column tiles, col/val
+    SPMM_FAMILY_COLTILE = 2,   /* a CTA per row block, warps own 128-column tiles, col/val
                                   staged in shared memory (wide N)                         */
+    SPMM_FAMILY_WINDOW = 3     /* persistent CTAs over contiguous row ranges; the B rows of a
+                                  sliding window [r0 - W, r1 + W) are streamed into shared
+                                  memory by bulk copies (column-locality graphs)           */
 } spmm_family;
 
 typedef struct spmm_plan_s *spmm_plan_t;
@@ -86,6 +89,13 @@ typedef struct {
     int32_t launches;       /* kernel launches one spmm_run makes                    */
     int32_t num_sms;        /* SM count the routing assumed                          */
     int64_t workspace_bytes;/* device scratch spmm_run needs for this (N, reduce)    */
+    /* column locality, known after spmm_plan_validate_cols (0 before) */
+    int64_t band_w;         /* smallest power of two W with >= 85% of entries at |col - row| <= W,
+                               0 if none up to 4096                                       */
+    double band_cover;      /* fraction of entries with |col - row| <= band_w           */
+    int32_t window_rows;    /* WINDOW family: rows per tile (0 for other families)      */
+    int32_t window_ctas;    /* WINDOW family: CTAs per column tile                      */
+    int64_t window_smem;    /* WINDOW family: dynamic shared memory per CTA, bytes      */
 } spmm_plan_info;
 
 /*
@@ -136,7 +146,10 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
 spmm_status spmm_plan_reserve(spmm_plan_t plan, int64_t N, spmm_reduce reduce);
 
 /*
- * spmm_plan_validate_cols -- check that every col[p], p < nnz, lies in [0, K).
+ * spmm_plan_validate_cols -- check that every col[p], p < nnz, lies in [0, K),
+ * and measure the column spread |col[p] - row(p)| (a log2 histogram) from
+ * which the router decides whether the WINDOW family applies. Until this has
+ * been called for a plan, the WINDOW family is not used.
  *   col : device, int32 [nnz]. Synchronous on `stream`.
  * Returns SPMM_ERR_INVALID_INPUT if any entry is out of range.
  */
@@ -167,8 +180,10 @@ spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split);
 /*
  * spmm_route -- the router as a pure host function. Reads the descriptor
  * fields of *desc (M, K, nnz, d_max, dbar, cv, t_split, chunk, n_heavy,
- * n_chunks) and fills the launch-shape fields of *out for (N, reduce) on a GPU
- * with `num_sms` SMs; `aligned` says whether B and C are 16-byte aligned.
+ * n_chunks, band_w, band_cover) and fills the launch-shape fields of *out for
+ * (N, reduce) on a GPU with `num_sms` SMs. `aligned` is a bit mask: bit 0 set
+ * when B, C (and argmax) are 16-byte aligned, bit 1 set when col (and val)
+ * are 16-byte aligned.
  * No CUDA call. (RA-SpMM "routing rules": first matching rule wins.)
  */
 spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce, int aligned,

@@ -34,7 +34,7 @@ __all__ = [
 ]
 
 REDUCE = {"sum": 0, "mean": 1, "max": 2}
-FAMILY = {"auto": -1, "rowgroup": 0, "warprow": 1, "coltile": 2}
+FAMILY = {"auto": -1, "rowgroup": 0, "warprow": 1, "coltile": 2, "window": 3}
 STATUS = {0: "SPMM_OK", 1: "SPMM_ERR_INVALID_ARG", 2: "SPMM_ERR_INVALID_INPUT", 3: "SPMM_ERR_OOM",
           4: "SPMM_ERR_CUDA", 5: "SPMM_ERR_UNSUPPORTED", 6: "SPMM_ERR_TIMEOUT"}
 
@@ -50,6 +50,9 @@ class PlanInfo(ctypes.Structure):
         ("vec", ctypes.c_int32), ("lanes", ctypes.c_int32), ("rows_per_warp", ctypes.c_int32),
         ("col_tiles", ctypes.c_int32), ("launches", ctypes.c_int32), ("num_sms", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
+        ("band_w", ctypes.c_int64), ("band_cover", ctypes.c_double),
+        ("window_rows", ctypes.c_int32), ("window_ctas", ctypes.c_int32),
+        ("window_smem", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
@@ -162,12 +165,15 @@ def spmm_plan_destroy(plan: int) -> None:
     _check(lib.spmm_plan_destroy(plan), "spmm_plan_destroy")
 
 
-def spmm_route(desc: dict, N: int, reduce: int, aligned: bool = True, num_sms: int = 152,
+def spmm_route(desc: dict, N: int, reduce: int, aligned: int = 3, num_sms: int = 152,
                family: int = -1) -> dict:
-    """The router as a pure host function (no GPU needed)."""
+    """The router as a pure host function (no GPU needed).
+
+    ``aligned``: bit 0 = B/C/argmax 16-byte aligned, bit 1 = col/val 16-byte aligned.
+    """
     d = PlanInfo()
     for k in ("M", "K", "nnz", "d_max", "n_empty", "dbar", "cv", "t_split", "chunk",
-              "n_heavy", "n_chunks"):
+              "n_heavy", "n_chunks", "band_w", "band_cover"):
         if k in desc:
             setattr(d, k, desc[k])
     out = PlanInfo()

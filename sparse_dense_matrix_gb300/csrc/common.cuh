@@ -41,7 +41,26 @@ struct Plan {
 
     int32_t *err = nullptr;          // device error words, see kErr*
     int family_override = SPMM_FAMILY_AUTO;
+
+    // column spread |col - row| measured by spmm_plan_validate_cols:
+    // spread_hist[b] counts entries with ceil(log2(|col - row|)) == b (0 for 0, 1)
+    bool spread_known = false;
+    int64_t spread_hist[34] = {0};
+    int64_t band_w = 0;              // window half-width chosen from the histogram (0: none)
+    double band_cover = 0.0;         // fraction of entries with |col - row| <= band_w
 };
+
+// Launch shape of the WINDOW family (host-computed; see f_window.cu).
+struct WinShape {
+    int R;          // rows per tile (one row per consumer lane group)
+    int W;          // window half-width: tile rows [r0, r1) stage B rows [r0 - W, r1 + W)
+    int cap;        // ring rows, >= 3R + 2W
+    int ecap;       // col/val entries staged per pipeline stage
+    int cw;         // B columns held per ring row (4 * lanes)
+    int Rp;         // row-pointer slots per stage (R + 1 rounded up to 4)
+    int off_meta, off_rp, off_col, off_val, off_ring, smem_bytes;
+};
+constexpr int kWindowSmemBudget = 227 * 1024;
 
 enum { kErrTimeout = 0, kErrBadCol = 1, kErrWords = 4 };
 
@@ -54,6 +73,8 @@ struct RunArgs {
     float *__restrict__ C;
     int32_t *__restrict__ argmax;
     int64_t M;
+    int64_t K;
+    int32_t nnz4;       // nnz rounded down to a multiple of 4
     int32_t N;          // feature width (columns of B and C)
     int32_t n_vec;      // N / vec
     int32_t t_split;    // light kernels skip rows with more entries than this
@@ -187,5 +208,9 @@ cudaError_t launch_warprow(const RunArgs &a, int vec, int lanes, int reduce, boo
                            int tiles, cudaStream_t s);
 cudaError_t launch_heavy(const RunArgs &a, int vec, int lanes, int reduce, bool has_val,
                          int tiles, cudaStream_t s);
+cudaError_t launch_window(const RunArgs &a, const WinShape &w, int lanes, int reduce, bool has_val,
+                          int grid_x, int tiles, cudaStream_t s);
+bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool has_val,
+                  int lanes, WinShape *out);
 
 }  // namespace spmm

@@ -151,14 +151,44 @@ __global__ void __launch_bounds__(kDescThreads) k_heavy_list(const int32_t *__re
     }
 }
 
-__global__ void k_check_cols(const int32_t *__restrict__ col, int64_t nnz, int64_t K,
-                             int32_t *__restrict__ err) {
+// Column check and column-spread histogram, one warp per row: every entry must
+// satisfy 0 <= col < K; |col - row| is binned by b = ceil(log2 |col - row|)
+// (b = 0 for distances 0 and 1). Warp-aggregated shared-memory counters, one
+// global add per bin per block (integer counts: the result is exact).
+constexpr int kSpreadBins = 34;
+__global__ void __launch_bounds__(256) k_check_cols(const int32_t *__restrict__ rowptr,
+                                                   const int32_t *__restrict__ col, int64_t M,
+                                                   int64_t K, int32_t *__restrict__ err,
+                                                   unsigned long long *__restrict__ hist) {
+    __shared__ unsigned int sh[kSpreadBins];
+    for (int b = threadIdx.x; b < kSpreadBins; b += blockDim.x) sh[b] = 0;
+    __syncthreads();
     int bad = 0;
-    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < nnz;
-         p += (int64_t)gridDim.x * blockDim.x) {
-        const int c = col[p];
-        bad |= (c < 0 || (int64_t)c >= K);
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < M;
+         row += warps) {
+        const int p0 = rowptr[row], p1 = rowptr[row + 1];
+        for (int pb = p0; pb < p1; pb += 32) {
+            const int p = pb + lane;
+            int b = -1;
+            if (p < p1) {
+                const int c = col[p];
+                if (c < 0 || (int64_t)c >= K) {
+                    bad = 1;
+                } else {
+                    const unsigned long long dist =
+                        (unsigned long long)((int64_t)c > row ? (int64_t)c - row : row - (int64_t)c);
+                    b = dist <= 1 ? 0 : 64 - __clzll((long long)(dist - 1));
+                }
+            }
+            const unsigned peers = __match_any_sync(__activemask(), b);
+            if (b >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sh[b], (unsigned)__popc(peers));
+        }
     }
+    __syncthreads();
+    for (int b = threadIdx.x; b < kSpreadBins; b += blockDim.x)
+        if (sh[b]) atomicAdd(&hist[b], (unsigned long long)sh[b]);
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err + kErrBadCol, 1);
 }
 
@@ -302,32 +332,67 @@ spmm_status ensure_workspace(Plan *p, size_t need) {
 
 // ------------------------------------------------------------------ router
 // Rules, first match wins (RA-SpMM "routing rules": descriptors + N -> family):
-//   R0  a family pinned by spmm_plan_set_family is used as given;
-//   R1  wide N (more than 32 column vectors per row)      -> WARPROW with column tiles;
-//   R2  near-uniform degrees (CV_d <= 1) and narrow N      -> ROWGROUP, 32/L rows per warp;
-//   R3  otherwise (skewed degrees)                          -> WARPROW.
+//   R0  a family pinned by spmm_plan_set_family is used as given (WINDOW only
+//       where its conditions hold);
+//   R1  column locality (>= 85% of entries within |col - row| <= W, W <= 4096,
+//       mean degree >= 2), N % 4 == 0 with 16-byte aligned operands, a ring of
+//       3R + 2W B rows that fits in shared memory with at most 4 column tiles,
+//       and a 2W halo below a quarter of a CTA's row range   -> WINDOW;
+//   R2  wide N (more than 32 column vectors per row)        -> WARPROW with column tiles;
+//   R3  near-uniform degrees (CV_d <= 1) and narrow N        -> ROWGROUP, 32/L rows per warp;
+//   R4  otherwise (skewed degrees)                            -> WARPROW.
 // Independently of the family, rows with more than t_split entries are split
 // into chunks (two extra launches) whenever the plan holds such rows.
+// `aligned`: bit 0 = B/C/argmax 16-byte aligned, bit 1 = col/val 16-byte aligned.
 static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int aligned, int num_sms,
                        int family_override, spmm_plan_info *o) {
     if (o != d) *o = *d;
     o->N = N;
     o->reduce = reduce;
     o->num_sms = num_sms;
-    o->vec = (aligned && N % 4 == 0) ? 4 : 1;
+    o->window_rows = 0;
+    o->window_ctas = 0;
+    o->window_smem = 0;
+    o->vec = ((aligned & 1) && N % 4 == 0) ? 4 : 1;
     const int64_t n_vec = (N + o->vec - 1) / o->vec;
-    const int64_t lanes = std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil(n_vec)));
+    int64_t lanes = std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil(n_vec)));
+    int fam = -2;
+    // R1: WINDOW
+    // (a pinned WINDOW skips the two efficiency conditions: mean degree and halo)
+    const bool forced = family_override == SPMM_FAMILY_WINDOW;
+    const bool window_ok = (family_override == SPMM_FAMILY_AUTO || forced) &&
+                           d->band_w > 0 && (aligned & 3) == 3 && N > 0 && N % 4 == 0 &&
+                           (forced || d->dbar >= 2.0) && d->M > 0;
+    if (window_ok) {
+        for (int64_t L = std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil((N + 3) / 4)));
+             L >= 2; L >>= 1) {
+            WinShape w;
+            if (!window_shape(d->M, d->K, N, d->dbar, d->band_w, true, (int)L, &w)) break;
+            if (w.smem_bytes > kWindowSmemBudget) continue;
+            const int64_t tiles_y = (N + 4 * L - 1) / (4 * L);
+            if (!forced && tiles_y > 4) break;
+            const int64_t ctas = std::max<int64_t>(1, (num_sms > 0 ? num_sms : 1) / tiles_y);
+            if (!forced && 4 * 2 * d->band_w > d->M / ctas) break;
+            fam = SPMM_FAMILY_WINDOW;
+            lanes = L;
+            o->window_rows = w.R;
+            o->window_ctas = (int32_t)ctas;
+            o->window_smem = w.smem_bytes;
+            break;
+        }
+    }
+    if (fam == -2) {
+        if (family_override != SPMM_FAMILY_AUTO && family_override != SPMM_FAMILY_WINDOW)
+            fam = family_override == SPMM_FAMILY_COLTILE ? SPMM_FAMILY_WARPROW : family_override;
+        else if (n_vec > 32)
+            fam = SPMM_FAMILY_WARPROW;
+        else if (d->cv <= 1.0)
+            fam = SPMM_FAMILY_ROWGROUP;
+        else
+            fam = SPMM_FAMILY_WARPROW;
+    }
     o->lanes = (int32_t)lanes;
     o->col_tiles = (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
-    int fam;
-    if (family_override != SPMM_FAMILY_AUTO)
-        fam = family_override == SPMM_FAMILY_COLTILE ? SPMM_FAMILY_WARPROW : family_override;
-    else if (n_vec > 32)
-        fam = SPMM_FAMILY_WARPROW;
-    else if (d->cv <= 1.0)
-        fam = SPMM_FAMILY_ROWGROUP;
-    else
-        fam = SPMM_FAMILY_WARPROW;
     o->family = fam;
     o->rows_per_warp = fam == SPMM_FAMILY_ROWGROUP ? (int32_t)(32 / lanes) : 1;
     o->launches = (d->M > 0 && N > 0) ? 1 + (d->n_heavy > 0 ? 2 : 0) : 0;
@@ -354,7 +419,7 @@ spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce
                        int num_sms, int family_override, spmm_plan_info *out) {
     if (!desc || !out || N < 0) return SPMM_ERR_INVALID_ARG;
     if (reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
-    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_COLTILE)
+    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_WINDOW)
         return SPMM_ERR_INVALID_ARG;
     route_fill(desc, N, reduce, aligned, num_sms, family_override, out);
     return SPMM_OK;
@@ -404,6 +469,8 @@ spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *
         st = from_cuda(e);
     } else if (ends[0] != 0 || ends[1] < 0) {
         st = SPMM_ERR_INVALID_INPUT;
+    } else if (ends[1] > INT32_MAX - 64) {
+        st = SPMM_ERR_UNSUPPORTED;
     } else {
         p->nnz = ends[1];
         p->t_split_default = spmm_default_t_split(M, p->nnz, p->num_sms);
@@ -436,18 +503,20 @@ static void fill_desc(const Plan *p, spmm_plan_info *o) {
     o->chunk = p->chunk;
     o->n_heavy = p->n_heavy;
     o->n_chunks = p->n_chunks;
+    o->band_w = p->band_w;
+    o->band_cover = p->band_cover;
 }
 
 spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce, spmm_plan_info *out) {
     if (!plan || !out || N < 0 || reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
     const Plan *p = reinterpret_cast<const Plan *>(plan);
     fill_desc(p, out);
-    route_fill(out, N, reduce, 1, p->num_sms, p->family_override, out);
+    route_fill(out, N, reduce, 3, p->num_sms, p->family_override, out);
     return SPMM_OK;
 }
 
 spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split) {
-    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_COLTILE) return SPMM_ERR_INVALID_ARG;
+    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_WINDOW) return SPMM_ERR_INVALID_ARG;
     Plan *p = reinterpret_cast<Plan *>(plan);
     p->family_override = family;
     const int64_t want = t_split > 0 ? t_split : p->t_split_default;
@@ -470,17 +539,43 @@ spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *
     if (!col) return SPMM_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     int32_t flag = 0;
-    cudaError_t e = cudaMemsetAsync(p->err + kErrBadCol, 0, sizeof(int32_t), s);
+    unsigned long long *d_hist = nullptr;
+    unsigned long long h_hist[kSpreadBins] = {0};
+    cudaError_t e = dev_alloc((void **)&d_hist, sizeof(h_hist));
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_hist, 0, sizeof(h_hist), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->err + kErrBadCol, 0, sizeof(int32_t), s);
     if (e == cudaSuccess) {
-        const int64_t blocks = std::min<int64_t>((p->nnz + 255) / 256, (int64_t)p->num_sms * 8);
-        k_check_cols<<<(unsigned)blocks, 256, 0, s>>>(col, p->nnz, p->K, p->err);
+        const int64_t blocks = std::min<int64_t>((p->M + 7) / 8, (int64_t)p->num_sms * 8);
+        k_check_cols<<<(unsigned)std::max<int64_t>(1, blocks), 256, 0, s>>>(p->rowptr, col, p->M,
+                                                                             p->K, p->err, d_hist);
         count_launch();
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = cudaMemcpyAsync(&flag, p->err + kErrBadCol, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h_hist, d_hist, sizeof(h_hist), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    dev_free(d_hist);
     if (e != cudaSuccess) return from_cuda(e);
-    return flag ? SPMM_ERR_INVALID_INPUT : SPMM_OK;
+    if (flag) return SPMM_ERR_INVALID_INPUT;
+    // window half-width: the smallest 2^b (b <= 12) holding >= 85% of the entries
+    unsigned long long total = 0, cum = 0;
+    for (int b = 0; b < kSpreadBins; ++b) {
+        p->spread_hist[b] = (int64_t)h_hist[b];
+        total += h_hist[b];
+    }
+    p->spread_known = true;
+    p->band_w = 0;
+    p->band_cover = 0.0;
+    for (int b = 0; b <= 12 && total > 0; ++b) {
+        cum += h_hist[b];
+        const double cover = (double)cum / (double)total;
+        if (b >= 1 && cover >= 0.85) {
+            p->band_w = (int64_t)1 << b;
+            p->band_cover = cover;
+            break;
+        }
+    }
+    return SPMM_OK;
 }
 
 spmm_status spmm_plan_sync(spmm_plan_t plan, void *stream) {
@@ -505,8 +600,9 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
     if (p->nnz > 0 && (!col || !B)) return SPMM_ERR_INVALID_ARG;
     if (N >= INT32_MAX / 4) return SPMM_ERR_UNSUPPORTED;
     if (reduce != SPMM_MAX) argmax = nullptr;
-    const int aligned = ((uintptr_t)B % 16 == 0) && ((uintptr_t)C % 16 == 0) &&
-                        ((uintptr_t)argmax % 16 == 0);
+    const int aligned = (((uintptr_t)B % 16 == 0) && ((uintptr_t)C % 16 == 0) &&
+                         ((uintptr_t)argmax % 16 == 0) ? 1 : 0) |
+                        (((uintptr_t)col % 16 == 0) && ((uintptr_t)val % 16 == 0) ? 2 : 0);
     spmm_plan_info r;
     fill_desc(p, &r);
     route_fill(&r, N, reduce, aligned, p->num_sms, p->family_override, &r);
@@ -521,6 +617,8 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
     a.C = C;
     a.argmax = argmax;
     a.M = p->M;
+    a.K = p->K;
+    a.nnz4 = (int32_t)(p->nnz & ~(int64_t)3);
     a.N = (int32_t)N;
     a.n_vec = (int32_t)((N + r.vec - 1) / r.vec);
     a.t_split = (int32_t)p->t_split;
@@ -542,7 +640,11 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
     }
     const bool has_val = val != nullptr;
     cudaError_t e;
-    if (r.family == SPMM_FAMILY_ROWGROUP)
+    if (r.family == SPMM_FAMILY_WINDOW) {
+        WinShape w;
+        window_shape(p->M, p->K, N, p->dbar, p->band_w, true, r.lanes, &w);
+        e = launch_window(a, w, r.lanes, reduce, has_val, r.window_ctas, r.col_tiles, s);
+    } else if (r.family == SPMM_FAMILY_ROWGROUP)
         e = launch_rowgroup(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
     else
         e = launch_warprow(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);

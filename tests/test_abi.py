@@ -122,3 +122,21 @@ def test_tensor_api_refuses_cpu_tensors(sdm):
     rp = torch.zeros(3, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         sdm.SparseAdj(rp, torch.zeros(0, dtype=torch.int32))
+
+
+def test_router_window_rule(sdm):
+    knn = dict(_desc(cv=0.0), band_w=512, band_cover=0.999)
+    r = sdm.spmm_route(knn, 16, 0)
+    assert (r["family_name"], r["lanes"], r["col_tiles"], r["window_rows"]) == ("window", 4, 1, 128)
+    assert 0 < r["window_smem"] <= 227 * 1024 and r["window_ctas"] == 152
+    r = sdm.spmm_route(knn, 64, 1)
+    assert (r["family_name"], r["lanes"], r["col_tiles"], r["window_ctas"]) == ("window", 8, 2, 76)
+    assert sdm.spmm_route(knn, 64, 0, aligned=1)["family_name"] == "rowgroup"   # col unaligned
+    assert sdm.spmm_route(knn, 18, 0)["family_name"] != "window"                 # N % 4 != 0
+    assert sdm.spmm_route(_desc(cv=0.0), 16, 0)["family_name"] == "rowgroup"    # spread unknown
+    small = dict(_desc(M=4096, nnz=40960, cv=0.0), band_w=512, band_cover=0.99)
+    assert sdm.spmm_route(small, 16, 0)["family_name"] == "rowgroup"            # halo too large
+    r = sdm.spmm_route(small, 16, 0, family=sdm.FAMILY["window"])
+    assert r["family_name"] == "window"                                           # pinned
+    wide = dict(_desc(cv=0.0), band_w=4096, band_cover=0.9)
+    assert sdm.spmm_route(wide, 512, 0)["family_name"] == "warprow"             # ring too big

@@ -243,3 +243,86 @@ def test_allocation_failure_is_reported(sdm, cuda_device, monkeypatch):
     B = gen.features(g.K, 16, seed=1)
     C, _ = gpu_reduce(adj, to_dev(B, cuda_device), "sum")
     compare(g, B, "sum", C, None)
+
+
+# ------------------------------------------------------------- WINDOW family
+def _banded_with_extras(M=20001, deg=10, window=64, seed=5):
+    """kNN-style band plus: 2 far-away columns on every 7th row (outside any
+    window), a block of long rows (overflows the staged entries of their
+    tile) and one row long enough to be split."""
+    g = gen.knn_local(M, deg, window, seed=seed, weighted=True)
+    rng = np.random.default_rng(seed)
+    rows = [list(g.col[g.rowptr[i]:g.rowptr[i + 1]]) for i in range(M)]
+    vals = [list(g.val[g.rowptr[i]:g.rowptr[i + 1]]) for i in range(M)]
+    for i in range(0, M, 7):
+        far = rng.integers(0, M, size=2).tolist()
+        rows[i] += far
+        vals[i] += rng.random(2).astype(np.float32).tolist()
+    for i in range(5000, 5100):
+        lo, hi = max(0, i - window), min(M, i + window + 1)
+        extra = rng.integers(lo, hi, size=100).tolist()
+        rows[i] += extra
+        vals[i] += rng.random(100).astype(np.float32).tolist()
+    rows[9000] = rng.integers(0, M, size=3001).tolist()
+    vals[9000] = rng.random(3001).astype(np.float32).tolist()
+    return gen.from_rows("banded_extras", M, M, rows, vals)
+
+
+@pytest.mark.parametrize("N", [4, 8, 16, 20, 32, 48, 64, 128, 256])
+def test_window_family_banded(sdm, cuda_device, N):
+    g = small("knn")
+    adj = make_adj(sdm, g, cuda_device)
+    adj.set_family("window")
+    info = adj.describe(N)
+    assert info["family_name"] == "window", info
+    assert info["band_w"] == 512
+    B = gen.features(g.K, N, seed=N + 100)
+    Bd = to_dev(B, cuda_device)
+    for red in ("sum", "mean", "max"):
+        C, A = gpu_reduce(adj, Bd, red)
+        compare(g, B, red, C, A, label=f"window knn N={N} {red}")
+    sdm.spmm_plan_sync(adj.plan)
+
+
+@pytest.mark.parametrize("N", [16, 36, 64, 128])
+def test_window_family_irregular(sdm, cuda_device, N):
+    g = _banded_with_extras()
+    assert g.nnz % 4 != 0
+    adj = make_adj(sdm, g, cuda_device)
+    adj.set_family("window")
+    info = adj.describe(N)
+    assert info["family_name"] == "window" and info["n_heavy"] == 1, info
+    B = gen.features(g.K, N, seed=N + 200)
+    Bd = to_dev(B, cuda_device)
+    for red in ("sum", "mean", "max"):
+        C, A = gpu_reduce(adj, Bd, red)
+        compare(g, B, red, C, A, label=f"window irregular N={N} {red}")
+    sdm.spmm_plan_sync(adj.plan)
+    # deterministic
+    import torch
+    r1, r2 = adj.reduce(Bd, "sum"), adj.reduce(Bd, "sum")
+    torch.cuda.synchronize()
+    assert torch.equal(r1.view(torch.int32), r2.view(torch.int32))
+
+
+def test_window_family_community_and_unaligned_col(sdm, cuda_device):
+    import torch
+    g = small("community")
+    adj = make_adj(sdm, g, cuda_device)
+    assert adj.describe(64)["band_w"] == 256
+    adj.set_family("window")
+    B = gen.features(g.K, 64, seed=3)
+    Bd = to_dev(B, cuda_device)
+    assert adj.describe(64)["family_name"] == "window"
+    for red in ("sum", "max"):
+        C, A = gpu_reduce(adj, Bd, red)
+        compare(g, B, red, C, A, label=f"window community {red}")
+    # col/val views that are not 16-byte aligned: the router must avoid WINDOW
+    cbuf = torch.empty(g.nnz + 1, dtype=torch.int32, device=cuda_device)
+    vbuf = torch.empty(g.nnz + 1, dtype=torch.float32, device=cuda_device)
+    cbuf[1:].copy_(to_dev(g.col, cuda_device))
+    vbuf[1:].copy_(to_dev(g.val, cuda_device))
+    adj2 = sdm.SparseAdj(to_dev(g.rowptr, cuda_device), cbuf[1:], vbuf[1:], num_cols=g.K)
+    adj2.set_family("window")
+    C, A = gpu_reduce(adj2, Bd, "sum")
+    compare(g, B, "sum", C, A, label="window unaligned col")
