@@ -164,7 +164,8 @@ spmm_status spmm_plan_sync(spmm_plan_t plan, void *stream);
 
 /*
  * spmm_plan_describe -- descriptors plus the routing decision spmm_run will
- * take for (N, reduce) with 16-byte aligned B and C. Host only, no CUDA call.
+ * take for (N, reduce) with 16-byte aligned B, C, col and val and a val array
+ * present. Host only, no CUDA call.
  */
 spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce,
                                spmm_plan_info *out);
@@ -183,7 +184,7 @@ spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split);
  * n_chunks, band_w, band_cover) and fills the launch-shape fields of *out for
  * (N, reduce) on a GPU with `num_sms` SMs. `aligned` is a bit mask: bit 0 set
  * when B, C (and argmax) are 16-byte aligned, bit 1 set when col (and val)
- * are 16-byte aligned.
+ * are 16-byte aligned, bit 2 set when there is no val array (unweighted).
  * No CUDA call. (RA-SpMM "routing rules": first matching rule wins.)
  */
 spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce, int aligned,

@@ -169,7 +169,8 @@ def spmm_route(desc: dict, N: int, reduce: int, aligned: int = 3, num_sms: int =
                family: int = -1) -> dict:
     """The router as a pure host function (no GPU needed).
 
-    ``aligned``: bit 0 = B/C/argmax 16-byte aligned, bit 1 = col/val 16-byte aligned.
+    ``aligned``: bit 0 = B/C/argmax 16-byte aligned, bit 1 = col/val 16-byte aligned,
+    bit 2 = no val array.
     """
     d = PlanInfo()
     for k in ("M", "K", "nnz", "d_max", "n_empty", "dbar", "cv", "t_split", "chunk",

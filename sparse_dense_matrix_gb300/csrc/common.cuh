@@ -24,7 +24,7 @@ struct Plan {
     int64_t d_max = 0, n_empty = 0;
     double dbar = 0.0, cv = 0.0;
 
-    int32_t *rowptr = nullptr;       // plan copy of rowptr [M+1]
+    int32_t *rowptr = nullptr;       // plan copy of rowptr [M+1], then kRowptrPad copies of rowptr[M]
 
     // heavy rows (d > t_split): ids ascending, chunk table (row, begin) per
     // chunk of `chunk` entries, first chunk of each heavy row (prefix, n_heavy+1)
@@ -47,20 +47,27 @@ struct Plan {
     bool spread_known = false;
     int64_t spread_hist[34] = {0};
     int64_t band_w = 0;              // window half-width chosen from the histogram (0: none)
+    bool band_all = false;           // every entry has |col - row| <= band_w
     double band_cover = 0.0;         // fraction of entries with |col - row| <= band_w
 };
 
 // Launch shape of the WINDOW family (host-computed; see f_window.cu).
 struct WinShape {
-    int R;          // rows per tile (one row per consumer lane group)
+    int R;          // rows per tile (two rows per consumer lane group)
     int W;          // window half-width: tile rows [r0, r1) stage B rows [r0 - W, r1 + W)
-    int cap;        // ring rows, >= 3R + 2W
+    int cap;        // ring rows, >= S R + 2W
+    int S;          // pipeline stages
     int ecap;       // col/val entries staged per pipeline stage
     int cw;         // B columns held per ring row (4 * lanes)
     int Rp;         // row-pointer slots per stage (R + 1 rounded up to 4)
+    int tmap;       // 1: ring rows are a column slice, loaded by 2-D tensor copies
+    int pow2;       // 1: cap is a power of two
+    int ctas_per_sm;// CTAs that fit on one SM (shared memory)
     int off_meta, off_rp, off_col, off_val, off_ring, smem_bytes;
 };
-constexpr int kWindowSmemBudget = 227 * 1024;
+constexpr int kWindowSmemBudget = 227 * 1024;   // per CTA
+constexpr int kWindowSmemPerSm = 228 * 1024;    // per SM
+constexpr int kRowptrPad = 1024;    // >= the largest row tile + 4
 
 enum { kErrTimeout = 0, kErrBadCol = 1, kErrWords = 4 };
 
@@ -178,8 +185,10 @@ struct Acc {
         }
     }
 
-    // final values for a row of d stored entries
+    // final values for a row of d stored entries (mean: one correctly rounded
+    // reciprocal of d per row, then a product per element)
     __device__ __forceinline__ void finish(int d, float (&out)[V], int (&arg)[V]) const {
+        const float inv_d = (RED == SPMM_MEAN && d > 0) ? __frcp_rn((float)d) : 0.0f;
 #pragma unroll
         for (int e = 0; e < V; ++e) {
             if constexpr (RED == SPMM_MAX) {
@@ -187,7 +196,7 @@ struct Acc {
                 out[e] = none ? 0.0f : v[e];
                 arg[e] = none ? -1 : j[e];
             } else if constexpr (RED == SPMM_MEAN) {
-                out[e] = d > 0 ? __fdiv_rn(v[e], (float)d) : 0.0f;
+                out[e] = __fmul_rn(v[e], inv_d);
                 arg[e] = 0;
             } else {
                 out[e] = v[e];
@@ -209,7 +218,7 @@ cudaError_t launch_warprow(const RunArgs &a, int vec, int lanes, int reduce, boo
 cudaError_t launch_heavy(const RunArgs &a, int vec, int lanes, int reduce, bool has_val,
                          int tiles, cudaStream_t s);
 cudaError_t launch_window(const RunArgs &a, const WinShape &w, int lanes, int reduce, bool has_val,
-                          int grid_x, int tiles, cudaStream_t s);
+                          bool check, int grid_x, int tiles, cudaStream_t s);
 bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool has_val,
                   int lanes, WinShape *out);
 

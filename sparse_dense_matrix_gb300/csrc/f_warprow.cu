@@ -149,8 +149,9 @@ __global__ void __launch_bounds__(128) k_heavy_combine(const RunArgs a) {
             }
         }
         if constexpr (RED == SPMM_MEAN) {
+            const float inv_d = __frcp_rn((float)d);
 #pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = __fdiv_rn(acc[e], (float)d);
+            for (int e = 0; e < V; ++e) acc[e] = __fmul_rn(acc[e], inv_d);
         }
         st_vec<V>(a.C + (int64_t)row * N + col0, acc);
         if constexpr (RED == SPMM_MAX) {

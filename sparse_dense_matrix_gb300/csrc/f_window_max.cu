@@ -1,0 +1,8 @@
+// WINDOW kernel instantiations for the max reduction.
+#include "window.cuh"
+
+namespace spmm {
+template cudaError_t launch_window_red<SPMM_MAX>(const RunArgs &, const WinShape &,
+                                              const CUtensorMap &, int, bool, bool, int, int,
+                                              cudaStream_t);
+}  // namespace spmm

@@ -337,13 +337,15 @@ spmm_status ensure_workspace(Plan *p, size_t need) {
 //   R1  column locality (>= 85% of entries within |col - row| <= W, W <= 4096,
 //       mean degree >= 2), N % 4 == 0 with 16-byte aligned operands, a ring of
 //       3R + 2W B rows that fits in shared memory with at most 4 column tiles,
-//       and a 2W halo below a quarter of a CTA's row range   -> WINDOW;
+//       an average tile's entries fitting one pipeline stage,
+//       and a 2W halo at most half of a CTA's row range        -> WINDOW;
 //   R2  wide N (more than 32 column vectors per row)        -> WARPROW with column tiles;
 //   R3  near-uniform degrees (CV_d <= 1) and narrow N        -> ROWGROUP, 32/L rows per warp;
 //   R4  otherwise (skewed degrees)                            -> WARPROW.
 // Independently of the family, rows with more than t_split entries are split
 // into chunks (two extra launches) whenever the plan holds such rows.
-// `aligned`: bit 0 = B/C/argmax 16-byte aligned, bit 1 = col/val 16-byte aligned.
+// `aligned`: bit 0 = B/C/argmax 16-byte aligned, bit 1 = col/val 16-byte aligned,
+// bit 2 = no val array (unweighted; the WINDOW family then stages no values).
 static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int aligned, int num_sms,
                        int family_override, spmm_plan_info *o) {
     if (o != d) *o = *d;
@@ -367,12 +369,17 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
         for (int64_t L = std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil((N + 3) / 4)));
              L >= 2; L >>= 1) {
             WinShape w;
-            if (!window_shape(d->M, d->K, N, d->dbar, d->band_w, true, (int)L, &w)) break;
+            if (!window_shape(d->M, d->K, N, d->dbar, d->band_w, !(aligned & 4), (int)L, &w))
+                break;
             if (w.smem_bytes > kWindowSmemBudget) continue;
+            // the staged entries of an average tile must fit a stage (else the
+            // tile is read from global memory)
+            if (!forced && (double)w.R * d->dbar * 1.25 + 64 > (double)w.ecap) break;
             const int64_t tiles_y = (N + 4 * L - 1) / (4 * L);
             if (!forced && tiles_y > 4) break;
-            const int64_t ctas = std::max<int64_t>(1, (num_sms > 0 ? num_sms : 1) / tiles_y);
-            if (!forced && 4 * 2 * d->band_w > d->M / ctas) break;
+            const int64_t ctas = std::max<int64_t>(
+                1, (num_sms > 0 ? num_sms : 1) * w.ctas_per_sm / tiles_y);
+            if (!forced && 2 * 2 * d->band_w > d->M / ctas) break;
             fam = SPMM_FAMILY_WINDOW;
             lanes = L;
             o->window_rows = w.R;
@@ -456,7 +463,7 @@ spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *
     spmm_status st = SPMM_OK;
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
-    if (e == cudaSuccess) e = dev_alloc((void **)&p->rowptr, sizeof(int32_t) * (M + 1));
+    if (e == cudaSuccess) e = dev_alloc((void **)&p->rowptr, sizeof(int32_t) * (M + 1 + kRowptrPad));
     if (e == cudaSuccess) e = dev_alloc((void **)&p->err, sizeof(int32_t) * kErrWords);
     if (e == cudaSuccess) e = cudaMemsetAsync(p->err, 0, sizeof(int32_t) * kErrWords, s);
     if (e == cudaSuccess)
@@ -473,6 +480,16 @@ spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *
         st = SPMM_ERR_UNSUPPORTED;
     } else {
         p->nnz = ends[1];
+        // pad the copy with rowptr[M] so that tile-sized bulk copies may run past row M
+        std::vector<int32_t> pad(kRowptrPad, ends[1]);
+        e = cudaMemcpyAsync(p->rowptr + M + 1, pad.data(), sizeof(int32_t) * kRowptrPad,
+                            cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) {
+            destroy(p);
+            t_alloc_countdown = 0;
+            return from_cuda(e);
+        }
         p->t_split_default = spmm_default_t_split(M, p->nnz, p->num_sms);
         st = analyse(p, p->t_split_default, s);
     }
@@ -572,6 +589,7 @@ spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *
         if (b >= 1 && cover >= 0.85) {
             p->band_w = (int64_t)1 << b;
             p->band_cover = cover;
+            p->band_all = (cum == total);
             break;
         }
     }
@@ -602,7 +620,8 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
     if (reduce != SPMM_MAX) argmax = nullptr;
     const int aligned = (((uintptr_t)B % 16 == 0) && ((uintptr_t)C % 16 == 0) &&
                          ((uintptr_t)argmax % 16 == 0) ? 1 : 0) |
-                        (((uintptr_t)col % 16 == 0) && ((uintptr_t)val % 16 == 0) ? 2 : 0);
+                        (((uintptr_t)col % 16 == 0) && ((uintptr_t)val % 16 == 0) ? 2 : 0) |
+                        (val == nullptr ? 4 : 0);
     spmm_plan_info r;
     fill_desc(p, &r);
     route_fill(&r, N, reduce, aligned, p->num_sms, p->family_override, &r);
@@ -642,8 +661,9 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
     cudaError_t e;
     if (r.family == SPMM_FAMILY_WINDOW) {
         WinShape w;
-        window_shape(p->M, p->K, N, p->dbar, p->band_w, true, r.lanes, &w);
-        e = launch_window(a, w, r.lanes, reduce, has_val, r.window_ctas, r.col_tiles, s);
+        window_shape(p->M, p->K, N, p->dbar, p->band_w, has_val, r.lanes, &w);
+        e = launch_window(a, w, r.lanes, reduce, has_val, !p->band_all, r.window_ctas,
+                          r.col_tiles, s);
     } else if (r.family == SPMM_FAMILY_ROWGROUP)
         e = launch_rowgroup(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
     else

@@ -5,6 +5,7 @@
 // broken invariant surfaces as SPMM_ERR_TIMEOUT instead of a hung GPU.
 #pragma once
 
+#include <cuda.h>
 #include <stdint.h>
 
 #include "common.cuh"
@@ -47,14 +48,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// One poll; a waiting thread may be suspended for up to kSuspendNs (it resumes
+// as soon as the phase completes), so waiting warps do not spin on the issue slots.
+constexpr uint32_t kSuspendNs = 100000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return done != 0;
 }
@@ -72,6 +76,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     return false;
 }
 
+// Shared-memory loads by 32-bit shared-window address (volatile: they stay
+// after the mbarrier wait that publishes the data).
+__device__ __forceinline__ int lds_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void lds_v4(uint32_t addr, float (&b)[4]) {
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(b[0]), "=f"(b[1]), "=f"(b[2]), "=f"(b[3])
+                 : "r"(addr));
+}
+
 // 1-D bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
 // from global memory into this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
@@ -79,6 +101,19 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// 2-D tiled tensor copy (box given by the tensor map) of the tile at element
+// coordinates (x, y) into this CTA's shared memory (128-byte aligned), completing
+// on `bar`. Rows or columns outside the tensor are filled with zeros.
+__device__ __forceinline__ void tensor2d_g2s(void *dst, const CUtensorMap *map, int x, int y,
+                                             uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(smem_addr(bar))
         : "memory");
 }
 

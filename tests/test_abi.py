@@ -127,10 +127,12 @@ def test_tensor_api_refuses_cpu_tensors(sdm):
 def test_router_window_rule(sdm):
     knn = dict(_desc(cv=0.0), band_w=512, band_cover=0.999)
     r = sdm.spmm_route(knn, 16, 0)
-    assert (r["family_name"], r["lanes"], r["col_tiles"], r["window_rows"]) == ("window", 4, 1, 128)
+    assert (r["family_name"], r["lanes"], r["col_tiles"], r["window_rows"]) == ("window", 4, 1, 256)
     assert 0 < r["window_smem"] <= 227 * 1024 and r["window_ctas"] == 152
     r = sdm.spmm_route(knn, 64, 1)
     assert (r["family_name"], r["lanes"], r["col_tiles"], r["window_ctas"]) == ("window", 8, 2, 76)
+    community = dict(_desc(M=65536, nnz=3668321, cv=0.1), band_w=256, band_cover=0.91)
+    assert sdm.spmm_route(community, 128, 0)["family_name"] != "window"          # stage overflow
     assert sdm.spmm_route(knn, 64, 0, aligned=1)["family_name"] == "rowgroup"   # col unaligned
     assert sdm.spmm_route(knn, 18, 0)["family_name"] != "window"                 # N % 4 != 0
     assert sdm.spmm_route(_desc(cv=0.0), 16, 0)["family_name"] == "rowgroup"    # spread unknown
