@@ -36,7 +36,13 @@ METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
 # DRAM bytes per launch of the dominant kernel from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel and the
 # workload; None until a capture of the current kernel exists.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/window_knn1M_bench.md (ncu --set full, first timed step)
+    "window/knn_1M/N16/sum": 149.0e6,
+    "window/knn_1M/N16/mean": 148.4e6,
+    "window/knn_1M/N64/sum": 558.9e6,
+    "window/knn_1M/N64/mean": 559.0e6,
+}
 
 FALLBACK_HBM_GBS = 6800.0
 
