@@ -196,6 +196,36 @@ spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce
  */
 int64_t spmm_default_t_split(int64_t M, int64_t nnz, int num_sms);
 
+/*
+ * spmm_run_noalloc -- the product of spmm_run, for callers that cannot
+ * allocate device memory: no plan, and no cudaMalloc / cudaFree or other
+ * allocating call on any path. The pages have no counterpart of this call;
+ * it exists for callers whose device memory is owned by another allocator
+ * (a framework's caching pool that a stray cudaMalloc would fragment or
+ * exhaust) and for serving loops that must not allocate after start-up
+ * (cudaMalloc and cudaFree synchronise the device and can fail at any time).
+ *   rowptr, col, val, B, C, argmax : as in spmm_plan_create and spmm_run,
+ *            all device pointers owned by the caller.
+ *   M, K, N, reduce, stream        : as in spmm_plan_create and spmm_run.
+ * Rows are reduced by the WARPROW family; rows longer than
+ * spmm_default_t_split(M, nnz, SMs) are split into chunks whose partials go to
+ * a file-scope device array of 64 MiB that every GPU which loads the library
+ * holds until the process exits. At most 65,536 split rows, 262,144 chunks and
+ * chunks x N x 4 bytes of partials (x 2 for SPMM_MAX) up to about 61 MiB fit
+ * in it; larger inputs return SPMM_ERR_UNSUPPORTED before any product kernel
+ * runs. rowptr[0] != 0 or a decreasing rowptr returns SPMM_ERR_INVALID_INPUT.
+ * Partly synchronous: nnz and the split-row counts are read back to the host
+ * (draining `stream`) before the product is enqueued.
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress; make that first call before any stream capture.
+ * Every call shares the one array and it keeps the last call's contents:
+ * calls whose GPU work overlaps (other streams, other host threads) race and
+ * must be serialised by the caller.
+ */
+spmm_status spmm_run_noalloc(const int32_t *rowptr, const int32_t *col, const float *val,
+                             const float *B, int64_t M, int64_t K, int64_t N, spmm_reduce reduce,
+                             float *C, int32_t *argmax, void *stream);
+
 /* spmm_plan_destroy -- free the plan and everything it owns. NULL is a no-op. */
 spmm_status spmm_plan_destroy(spmm_plan_t plan);
 

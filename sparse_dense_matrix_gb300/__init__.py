@@ -30,6 +30,7 @@ __all__ = [
     "spmm_plan_create", "spmm_run", "spmm_plan_describe", "spmm_plan_destroy",
     "spmm_plan_reserve", "spmm_plan_validate_cols", "spmm_plan_sync", "spmm_plan_set_family",
     "spmm_route", "spmm_default_t_split", "spmm_status_string", "spmm_launch_count",
+    "spmm_run_noalloc",
     "PlanInfo", "REDUCE", "FAMILY", "lib", "build_library",
 ]
 
@@ -89,6 +90,7 @@ def _load():
         "spmm_plan_destroy": ([vp], i32),
         "spmm_status_string": ([i32], ctypes.c_char_p),
         "spmm_launch_count": ([], ctypes.c_uint64),
+        "spmm_run_noalloc": ([vp, vp, vp, vp, i64, i64, i64, i32, vp, vp, vp], i32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(L, name)
@@ -181,6 +183,13 @@ def spmm_route(desc: dict, N: int, reduce: int, aligned: int = 3, num_sms: int =
     _check(lib.spmm_route(ctypes.byref(d), N, reduce, int(aligned), num_sms, family,
                           ctypes.byref(out)), "spmm_route")
     return out.as_dict()
+
+
+def spmm_run_noalloc(rowptr_ptr: int, col_ptr: int, val_ptr, B_ptr: int, M: int, K: int, N: int,
+                     reduce: int, C_ptr: int, argmax_ptr=None, stream=None) -> None:
+    """spmm_run without a plan and without device allocation (see include/spmm.h)."""
+    _check(lib.spmm_run_noalloc(rowptr_ptr, col_ptr, val_ptr, B_ptr, M, K, N, reduce, C_ptr,
+                                argmax_ptr, _stream_handle(stream)), "spmm_run_noalloc")
 
 
 # ------------------------------------------------------------ tensor API
