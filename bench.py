@@ -118,9 +118,9 @@ class ClockSampler:
         self.path = None
         if shutil.which("nvidia-smi") is None:
             return
-        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
-        self.f = open(self.path, "w")
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="spmm_clocks_", suffix=".csv")
+        self.f = os.fdopen(fd, "w")
         self.proc = subprocess.Popen(
             ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
              "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
@@ -135,9 +135,12 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
+        with open(self.path) as f:
+            lines = f.readlines()
+        os.unlink(self.path)
         sm, smax, reasons, n = [], None, set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
