@@ -220,6 +220,6 @@ cudaError_t launch_heavy(const RunArgs &a, int vec, int lanes, int reduce, bool 
 cudaError_t launch_window(const RunArgs &a, const WinShape &w, int lanes, int reduce, bool has_val,
                           bool check, int grid_x, int tiles, cudaStream_t s);
 bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool has_val,
-                  int lanes, WinShape *out);
+                  int lanes, int rows_per_group, WinShape *out);
 
 }  // namespace spmm

@@ -32,11 +32,14 @@ static void window_layout(WinShape &w, bool has_val, int S) {
 }
 
 bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool has_val,
-                  int lanes, WinShape *o) {
+                  int lanes, int rows_per_group, WinShape *o) {
     (void)M; (void)K;
     if (lanes < 2 || lanes > 32 || W < 0 || N <= 0) return false;
+    if (rows_per_group < 1 || rows_per_group > 2) return false;
     WinShape w{};
-    w.R = 2 * kWinConsumerWarps * kWarp / lanes;   // two rows per lane group
+    // one or two rows per lane group (two keep more gathers in flight; one keeps
+    // the staged entries of high-degree tiles within a stage)
+    w.R = rows_per_group * kWinConsumerWarps * kWarp / lanes;
     w.cw = 4 * lanes;
     // a column slice of B comes by 2-D tensor copies of R-row boxes: W and cap
     // are then multiples of R so that boxes start on a multiple of R and never

@@ -334,11 +334,12 @@ spmm_status ensure_workspace(Plan *p, size_t need) {
 // Rules, first match wins (RA-SpMM "routing rules": descriptors + N -> family):
 //   R0  a family pinned by spmm_plan_set_family is used as given (WINDOW only
 //       where its conditions hold);
-//   R1  column locality (>= 85% of entries within |col - row| <= W, W <= 4096,
-//       mean degree >= 2), N % 4 == 0 with 16-byte aligned operands, a ring of
+//   R1  column locality (>= 97% of entries within |col - row| <= W, W <= 4096,
+//       mean degree >= 2; an out-of-window gather stalls its whole batch), N % 4 == 0 with 16-byte aligned operands, a ring of
 //       3R + 2W B rows that fits in shared memory with at most 4 column tiles,
-//       an average tile's entries fitting one pipeline stage,
-//       and a 2W halo at most half of a CTA's row range        -> WINDOW;
+//       an average tile's entries fitting one pipeline stage (two rows per
+//       lane group preferred, else one), and a 2W halo at most twice a CTA's
+//       row range                                              -> WINDOW;
 //   R2  wide N (more than 32 column vectors per row)        -> WARPROW with column tiles;
 //   R3  near-uniform degrees (CV_d <= 1) and narrow N        -> ROWGROUP, 32/L rows per warp;
 //   R4  otherwise (skewed degrees)                            -> WARPROW.
@@ -364,28 +365,34 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     const bool forced = family_override == SPMM_FAMILY_WINDOW;
     const bool window_ok = (family_override == SPMM_FAMILY_AUTO || forced) &&
                            d->band_w > 0 && (aligned & 3) == 3 && N > 0 && N % 4 == 0 &&
-                           (forced || d->dbar >= 2.0) && d->M > 0;
+                           (forced || (d->dbar >= 2.0 && d->band_cover >= 0.97)) && d->M > 0;
     if (window_ok) {
+        bool found = false;
         for (int64_t L = std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil((N + 3) / 4)));
-             L >= 2; L >>= 1) {
-            WinShape w;
-            if (!window_shape(d->M, d->K, N, d->dbar, d->band_w, !(aligned & 4), (int)L, &w))
-                break;
-            if (w.smem_bytes > kWindowSmemBudget) continue;
-            // the staged entries of an average tile must fit a stage (else the
-            // tile is read from global memory)
-            if (!forced && (double)w.R * d->dbar * 1.25 + 64 > (double)w.ecap) break;
-            const int64_t tiles_y = (N + 4 * L - 1) / (4 * L);
-            if (!forced && tiles_y > 4) break;
-            const int64_t ctas = std::max<int64_t>(
-                1, (num_sms > 0 ? num_sms : 1) * w.ctas_per_sm / tiles_y);
-            if (!forced && 2 * 2 * d->band_w > d->M / ctas) break;
-            fam = SPMM_FAMILY_WINDOW;
-            lanes = L;
-            o->window_rows = w.R;
-            o->window_ctas = (int32_t)ctas;
-            o->window_smem = w.smem_bytes;
-            break;
+             L >= 2 && !found; L >>= 1) {
+            for (int rpg = 2; rpg >= 1 && !found; --rpg) {
+                WinShape w;
+                if (!window_shape(d->M, d->K, N, d->dbar, d->band_w, !(aligned & 4), (int)L, rpg,
+                                  &w))
+                    continue;
+                if (w.smem_bytes > kWindowSmemBudget) continue;
+                // the staged entries of an average tile must fit a stage (else the
+                // tile is read from global memory)
+                if (!forced && (double)w.R * d->dbar * 1.25 + 64 > (double)w.ecap) continue;
+                const int64_t tiles_y = (N + 4 * L - 1) / (4 * L);
+                if (!forced && tiles_y > 4) continue;
+                const int64_t ctas = std::max<int64_t>(
+                    1, (num_sms > 0 ? num_sms : 1) * w.ctas_per_sm / tiles_y);
+                // the halo rows come from L2 (neighbouring CTAs stream them too):
+                // allow a halo up to twice a CTA's own rows
+                if (!forced && 2 * d->band_w > 2 * (d->M / ctas)) continue;
+                fam = SPMM_FAMILY_WINDOW;
+                lanes = L;
+                o->window_rows = w.R;
+                o->window_ctas = (int32_t)ctas;
+                o->window_smem = w.smem_bytes;
+                found = true;
+            }
         }
     }
     if (fam == -2) {
@@ -661,7 +668,8 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
     cudaError_t e;
     if (r.family == SPMM_FAMILY_WINDOW) {
         WinShape w;
-        window_shape(p->M, p->K, N, p->dbar, p->band_w, has_val, r.lanes, &w);
+        const int rpg = (int)((int64_t)r.window_rows * r.lanes / (kWarp * 16));
+        window_shape(p->M, p->K, N, p->dbar, p->band_w, has_val, r.lanes, rpg, &w);
         e = launch_window(a, w, r.lanes, reduce, has_val, !p->band_all, r.window_ctas,
                           r.col_tiles, s);
     } else if (r.family == SPMM_FAMILY_ROWGROUP)

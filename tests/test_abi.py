@@ -132,7 +132,11 @@ def test_router_window_rule(sdm):
     r = sdm.spmm_route(knn, 64, 1)
     assert (r["family_name"], r["lanes"], r["col_tiles"], r["window_ctas"]) == ("window", 8, 2, 76)
     community = dict(_desc(M=65536, nnz=3668321, cv=0.1), band_w=256, band_cover=0.91)
-    assert sdm.spmm_route(community, 128, 0)["family_name"] != "window"          # stage overflow
+    assert sdm.spmm_route(community, 128, 0)["family_name"] != "window"          # 9% outside W
+    dense_band = dict(community, band_cover=0.99)   # high degree: one row per lane group
+    r = sdm.spmm_route(dense_band, 128, 0)
+    assert (r["family_name"], r["lanes"], r["window_rows"]) == ("window", 16, 32)
+    assert sdm.spmm_route(dense_band, 512, 0)["family_name"] != "window"         # ring too big
     assert sdm.spmm_route(knn, 64, 0, aligned=1)["family_name"] == "rowgroup"   # col unaligned
     assert sdm.spmm_route(knn, 18, 0)["family_name"] != "window"                 # N % 4 != 0
     assert sdm.spmm_route(_desc(cv=0.0), 16, 0)["family_name"] == "rowgroup"    # spread unknown
