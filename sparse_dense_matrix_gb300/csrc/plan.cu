@@ -335,8 +335,9 @@ spmm_status ensure_workspace(Plan *p, size_t need) {
 //   R0  a family pinned by spmm_plan_set_family is used as given (WINDOW only
 //       where its conditions hold);
 //   R1  column locality (>= 97% of entries within |col - row| <= W, W <= 4096,
-//       mean degree >= 2; an out-of-window gather stalls its whole batch), N % 4 == 0 with 16-byte aligned operands, a ring of
-//       3R + 2W B rows that fits in shared memory with at most 4 column tiles,
+//       mean degree >= 2; an out-of-window gather stalls its whole batch),
+//       N % 4 == 0 with 16-byte aligned operands, a ring of 3R + 2W B rows
+//       that fits in shared memory with at most 4 column tiles,
 //       an average tile's entries fitting one pipeline stage (two rows per
 //       lane group preferred, else one), and a 2W halo at most twice a CTA's
 //       row range                                              -> WINDOW;
