@@ -342,36 +342,56 @@ def run_ours(args):
                         "gflops": 2.0 * g.nnz * n / (np.median(per_run_ms[:, k]) / 1e3) / 1e9,
                         "hbm_frac": b / (np.median(per_run_ms[:, k]) / 1e3) / 1e9 / hbm_peak})
 
-    # end to end through the public API with pinned host buffers
+    # End to end through the public API with pinned host buffers: every step
+    # copies each feature matrix in once (one per N) and every result out; the
+    # copies run on their own streams and overlap the other runs' kernels.
     e2e = None
     if not args.no_e2e:
         Bh = {n: torch.from_numpy(B_host[n]).pin_memory() for n in Ns}
-        Ch = {n: torch.empty((g.M, n), dtype=torch.float32).pin_memory() for n in Ns}
-        Ah = {n: torch.empty((g.M, n), dtype=torch.int32).pin_memory() for n in Ns}
-        h2d = sum(g.K * n * 4 for n, _ in runs)
+        Ch = [torch.empty((g.M, n), dtype=torch.float32).pin_memory() for n, _ in runs]
+        Ah = [torch.empty((g.M, n), dtype=torch.int32).pin_memory() if r == "max" else None
+              for n, r in runs]
+        Cr = [torch.empty((g.M, n), dtype=torch.float32, device=dev) for n, _ in runs]
+        Ar = [torch.empty((g.M, n), dtype=torch.int32, device=dev) if r == "max" else None
+              for n, r in runs]
+        h2d = sum(g.K * n * 4 for n in Ns)
         d2h = sum(g.M * n * 4 * (2 if r == "max" else 1) for n, r in runs)
         e2e_steps = max(3, min(args.steps, 50))
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
         def e2e_step():
-            for n, r in runs:
-                Bd[n].copy_(Bh[n], non_blocking=True)
-                res = adj.reduce(Bd[n], r, out=Cd[n], argmax=Ad[n] if r == "max" else None)
-                Ch[n].copy_(Cd[n], non_blocking=True)
-                if r == "max":
-                    Ah[n].copy_(res[1], non_blocking=True)
+            ready = {}
+            for n in Ns:
+                with torch.cuda.stream(s_in):
+                    Bd[n].copy_(Bh[n], non_blocking=True)
+                    ready[n] = torch.cuda.Event()
+                    ready[n].record(s_in)
+            for k, (n, r) in enumerate(runs):
+                stream.wait_event(ready[n])
+                adj.reduce(Bd[n], r, out=Cr[k], argmax=Ar[k], stream=stream)
+                done = torch.cuda.Event()
+                done.record(stream)
+                s_out.wait_event(done)
+                with torch.cuda.stream(s_out):
+                    Ch[k].copy_(Cr[k], non_blocking=True)
+                    if Ar[k] is not None:
+                        Ah[k].copy_(Ar[k], non_blocking=True)
+            # the next step's inputs overwrite Bd: wait for this step's kernels
+            s_in.wait_stream(stream)
+            stream.wait_stream(s_out)
+
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        t_e0 = time.perf_counter()
         for _ in range(e2e_steps):
             e2e_step()
-        b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b)
+        e2e_ms = (time.perf_counter() - t_e0) * 1e3
         e2e = {"value": flops_step * e2e_steps * world / (e2e_ms / 1e3) / 1e9, "unit": "GFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps}
+               "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+               "timing": "wall clock, synchronised on both sides; copies overlap kernels"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
