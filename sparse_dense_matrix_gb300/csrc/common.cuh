@@ -217,6 +217,8 @@ cudaError_t launch_warprow(const RunArgs &a, int vec, int lanes, int reduce, boo
                            int tiles, cudaStream_t s);
 cudaError_t launch_heavy(const RunArgs &a, int vec, int lanes, int reduce, bool has_val,
                          int tiles, cudaStream_t s);
+cudaError_t launch_coltile(const RunArgs &a, int wpr, int tiles_y, int reduce, bool has_val,
+                           bool bulk_ok, cudaStream_t s);
 cudaError_t launch_window(const RunArgs &a, const WinShape &w, int lanes, int reduce, bool has_val,
                           bool check, int grid_x, int tiles, cudaStream_t s);
 bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool has_val,

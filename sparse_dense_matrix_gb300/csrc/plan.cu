@@ -341,7 +341,8 @@ spmm_status ensure_workspace(Plan *p, size_t need) {
 //       an average tile's entries fitting one pipeline stage (two rows per
 //       lane group preferred, else one), and a 2W halo at most twice a CTA's
 //       row range                                              -> WINDOW;
-//   R2  wide N (more than 32 column vectors per row)        -> WARPROW with column tiles;
+//   R2  wide N (more than 32 column vectors per row)        -> WARPROW with column
+//       tiles (COLTILE, the staged variant, measured 1.1-1.7x slower: pin only);
 //   R3  near-uniform degrees (CV_d <= 1) and narrow N        -> ROWGROUP, 32/L rows per warp;
 //   R4  otherwise (skewed degrees)                            -> WARPROW.
 // Independently of the family, rows with more than t_split entries are split
@@ -396,16 +397,21 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
             }
         }
     }
+    // COLTILE needs 128-bit vectors (N % 4 == 0, aligned B/C); else WARPROW tiles
+    const bool coltile_ok = o->vec == 4;
     if (fam == -2) {
-        if (family_override != SPMM_FAMILY_AUTO && family_override != SPMM_FAMILY_WINDOW)
-            fam = family_override == SPMM_FAMILY_COLTILE ? SPMM_FAMILY_WARPROW : family_override;
+        if (family_override == SPMM_FAMILY_COLTILE)
+            fam = coltile_ok ? SPMM_FAMILY_COLTILE : SPMM_FAMILY_WARPROW;
+        else if (family_override != SPMM_FAMILY_AUTO && family_override != SPMM_FAMILY_WINDOW)
+            fam = family_override;
         else if (n_vec > 32)
-            fam = SPMM_FAMILY_WARPROW;
+            fam = SPMM_FAMILY_WARPROW;   // measured faster than COLTILE on the wide workloads
         else if (d->cv <= 1.0)
             fam = SPMM_FAMILY_ROWGROUP;
         else
             fam = SPMM_FAMILY_WARPROW;
     }
+    if (fam == SPMM_FAMILY_COLTILE) lanes = 32;     // one 128-column tile per warp
     o->lanes = (int32_t)lanes;
     o->col_tiles = (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
     o->family = fam;
@@ -673,6 +679,13 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
         window_shape(p->M, p->K, N, p->dbar, p->band_w, has_val, r.lanes, rpg, &w);
         e = launch_window(a, w, r.lanes, reduce, has_val, !p->band_all, r.window_ctas,
                           r.col_tiles, s);
+    } else if (r.family == SPMM_FAMILY_COLTILE) {
+        // warps per row: the column tiles, up to a CTA's 8 warps (a power of two)
+        int wpr = 1;
+        while (wpr < r.col_tiles && wpr < 8) wpr <<= 1;
+        const int tiles_y = (r.col_tiles + wpr - 1) / wpr;
+        if (tiles_y > kMaxTilesY) return SPMM_ERR_UNSUPPORTED;
+        e = launch_coltile(a, wpr, tiles_y, reduce, has_val, (aligned & 2) != 0, s);
     } else if (r.family == SPMM_FAMILY_ROWGROUP)
         e = launch_rowgroup(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
     else

@@ -88,12 +88,17 @@ def test_router_rules(sdm):
     assert (r["family_name"], r["lanes"], r["rows_per_warp"]) == ("warprow", 16, 1)
     r = sdm.spmm_route(_desc(cv=0.1), 512, 0)                 # wide N: column tiles
     assert (r["family_name"], r["vec"], r["lanes"], r["col_tiles"]) == ("warprow", 4, 32, 4)
+    r = sdm.spmm_route(_desc(cv=0.1), 512, 0, aligned=0)      # no 128-bit vectors
+    assert (r["family_name"], r["vec"], r["col_tiles"]) == ("warprow", 1, 16)
+    r = sdm.spmm_route(_desc(cv=0.1), 64, 0, family=sdm.FAMILY["coltile"])
+    assert (r["family_name"], r["lanes"], r["col_tiles"]) == ("coltile", 32, 1)
     r = sdm.spmm_route(_desc(cv=0.0), 16, 0, aligned=False)    # scalar path
     assert (r["vec"], r["lanes"], r["rows_per_warp"]) == (1, 16, 2)
     r = sdm.spmm_route(_desc(cv=0.0), 17, 0)                   # N % 4 != 0
     assert (r["vec"], r["lanes"], r["col_tiles"]) == (1, 32, 1)
     r = sdm.spmm_route(_desc(cv=0.0), 33, 0)
     assert (r["family_name"], r["vec"], r["col_tiles"]) == ("warprow", 1, 2)
+    assert sdm.spmm_route(_desc(cv=0.0), 36, 0)["family_name"] == "rowgroup"
     r = sdm.spmm_route(_desc(cv=0.0), 1, 2)
     assert (r["vec"], r["lanes"], r["rows_per_warp"]) == (1, 2, 16)
     r = sdm.spmm_route(_desc(cv=0.0), 16, 0, family=sdm.FAMILY["warprow"])

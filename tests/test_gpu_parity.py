@@ -67,7 +67,46 @@ def test_forced_families_and_splits(sdm, cuda_device, family, t_split, N):
         compare(g, B, red, C, A, label=f"{family} t={t_split} N={N} {red}")
 
 
-@pytest.mark.parametrize("family", ["auto", "rowgroup", "warprow"])
+@pytest.mark.parametrize("t_split", [0, 24])
+@pytest.mark.parametrize("N", [128, 132, 256, 384, 520, 1040])
+def test_coltile_family(sdm, cuda_device, t_split, N):
+    """COLTILE (wide N): staged col/val, bulk copies for long aligned segments,
+    padding between rows, tiles beyond N, split rows, ragged N (scalar fallback)."""
+    g = small("rmat")
+    B = gen.features(g.K, N, seed=N + 5)
+    adj = make_adj(sdm, g, cuda_device)
+    adj.set_family("coltile", t_split)
+    info = adj.describe(N)
+    assert info["family_name"] == ("coltile" if N % 4 == 0 else "warprow")
+    Bd = to_dev(B, cuda_device)
+    for red in ("sum", "mean", "max"):
+        C, A = gpu_reduce(adj, Bd, red)
+        compare(g, B, red, C, A, label=f"coltile t={t_split} N={N} {red}")
+    sdm.spmm_plan_sync(adj.plan)
+
+
+def test_coltile_unaligned_col_and_long_rows(sdm, cuda_device):
+    import torch
+    g = small("chung_lu")                          # rows up to thousands of entries
+    B = gen.features(g.K, 256, seed=17)
+    Bd = to_dev(B, cuda_device)
+    for aligned in (True, False):
+        if aligned:
+            adj = make_adj(sdm, g, cuda_device)
+        else:
+            cb = torch.empty(g.nnz + 1, dtype=torch.int32, device=cuda_device)
+            vb = torch.empty(g.nnz + 1, dtype=torch.float32, device=cuda_device)
+            cb[1:].copy_(to_dev(g.col, cuda_device))
+            vb[1:].copy_(to_dev(g.val, cuda_device))
+            adj = sdm.SparseAdj(to_dev(g.rowptr, cuda_device), cb[1:], vb[1:], num_cols=g.K)
+        adj.set_family("coltile", 4000)            # long light rows: bulk copies, many chunks
+        for red in ("sum", "max"):
+            C, A = gpu_reduce(adj, Bd, red)
+            compare(g, B, red, C, A, label=f"coltile long rows aligned={aligned} {red}")
+        sdm.spmm_plan_sync(adj.plan)
+
+
+@pytest.mark.parametrize("family", ["auto", "rowgroup", "warprow", "coltile"])
 @pytest.mark.parametrize("t_split", [0, 16])
 def test_bitwise_deterministic(sdm, cuda_device, family, t_split):
     import torch
