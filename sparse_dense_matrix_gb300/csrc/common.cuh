@@ -141,6 +141,15 @@ __device__ __forceinline__ void st_vec_i(int32_t *p, const int (&x)[V]) {
 
 constexpr int kNoCol = INT_MAX;
 
+// Reciprocal by the PTX rcp.approx.f32 instruction (at most 1 ulp from 1/x);
+// the mean is then fl(sum * rcp(d)), a few ulp from the correctly rounded
+// quotient, far inside the sum/mean tolerance.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ bool max_better(float y, int jy, float v, int jv) {
     return y > v || (y == v && jy < jv);
 }
@@ -185,10 +194,10 @@ struct Acc {
         }
     }
 
-    // final values for a row of d stored entries (mean: one correctly rounded
-    // reciprocal of d per row, then a product per element)
+    // final values for a row of d stored entries (mean: one reciprocal of d per
+    // row, then a product per element)
     __device__ __forceinline__ void finish(int d, float (&out)[V], int (&arg)[V]) const {
-        const float inv_d = (RED == SPMM_MEAN && d > 0) ? __frcp_rn((float)d) : 0.0f;
+        const float inv_d = (RED == SPMM_MEAN && d > 0) ? rcp_approx((float)d) : 0.0f;
 #pragma unroll
         for (int e = 0; e < V; ++e) {
             if constexpr (RED == SPMM_MAX) {

@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(128) k_heavy_combine(const RunArgs a) {
             }
         }
         if constexpr (RED == SPMM_MEAN) {
-            const float inv_d = __frcp_rn((float)d);
+            const float inv_d = rcp_approx((float)d);
 #pragma unroll
             for (int e = 0; e < V; ++e) acc[e] = __fmul_rn(acc[e], inv_d);
         }

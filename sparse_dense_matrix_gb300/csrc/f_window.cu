@@ -50,29 +50,21 @@ bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool 
     int64_t ecap = (int64_t)(w.R * dbar * 1.25) + 64;
     ecap = std::min<int64_t>(4096, std::max<int64_t>(256, (ecap + 3) & ~3));
     w.ecap = (int)ecap;
-    // Pipeline depth: the bytes in flight per SM are about CTAs x (S - 1) tiles.
-    // Prefer two CTAs per SM with at least 3 stages, else one CTA with as many
-    // stages (up to 8) as fit.
-    const int half = kWindowSmemPerSm / 2 - 1024;
-    int S = 0, ctas = 0;
+    // Pipeline depth: one CTA per SM (the consumer warps need more than half of
+    // an SM's registers), with as many stages (3 to 8) as shared memory holds.
+    int S = 0;
     for (int s = kWinMaxStages; s >= 3 && !S; --s) {
         window_layout(w, has_val, s);
-        if (w.smem_bytes <= half) { S = s; ctas = 2; }
+        if (w.smem_bytes <= kWindowSmemBudget) S = s;
     }
-    if (!S) {
-        for (int s = kWinMaxStages; s >= 3 && !S; --s) {
-            window_layout(w, has_val, s);
-            if (w.smem_bytes <= kWindowSmemBudget) { S = s; ctas = 1; }
-        }
-    }
-    if (!S) S = 3, ctas = 1;                        // too large: the caller rejects it
+    if (!S) S = 3;                                   // too large: the caller rejects it
     window_layout(w, has_val, S);
-    w.ctas_per_sm = ctas;
+    w.ctas_per_sm = 1;
     // a power-of-two ring turns the slot of row j into j & (cap - 1)
     int cap2 = 1;
     while (cap2 < w.cap) cap2 <<= 1;
     const int64_t pow2_bytes = (int64_t)w.smem_bytes + (int64_t)(cap2 - w.cap) * w.cw * 4;
-    if (pow2_bytes <= (ctas == 2 ? half : kWindowSmemBudget)) {
+    if (pow2_bytes <= kWindowSmemBudget) {
         w.cap = cap2;
         w.pow2 = 1;
         w.smem_bytes = (int)pow2_bytes;

@@ -32,7 +32,7 @@ constexpr int kWinConsumerWarps = 16;
 constexpr int kWinThreads = (kWinConsumerWarps + 1) * kWarp;
 
 template <int L, int RED, bool HAS_VAL, bool CHECK, bool POW2>
-__global__ void __launch_bounds__(kWinThreads, 2)
+__global__ void __launch_bounds__(kWinThreads, 1)
     k_window(const RunArgs a, const WinShape w, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // 128-byte aligned base (tensor copies want 128-byte aligned destinations)
