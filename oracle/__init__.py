@@ -16,6 +16,11 @@ section 2, Algorithm 1):
 
 ``T`` (returned for sum/mean) is sum_p |a_p * B[col_p, k]|, the scale of the
 tolerance |err| <= 1e-5 * T + 1e-6.
+
+Backward (graph-spmm card, "Requirements and limits" and "API"): ``transpose``
+builds A^T in CSR (stable by row; optionally each value divided by its row's
+degree, for the mean), so that the sum / mean backward is a product with it;
+``maxpool_backward`` routes dC[i, k] to the forward argmax column.
 """
 from __future__ import annotations
 
@@ -73,6 +78,10 @@ class Oracle:
         lib.oracle_descriptors.argtypes = [i64, p, ctypes.POINTER(_Desc)]
         lib.oracle_descriptors.restype = ctypes.c_int
         lib.oracle_threads.restype = ctypes.c_int
+        lib.oracle_transpose.argtypes = [i64, i64, p, p, p, ctypes.c_int, p, p, p]
+        lib.oracle_transpose.restype = ctypes.c_int
+        lib.oracle_maxpool_backward.argtypes = [i64, i64, i64, p, p, p, p, p, p]
+        lib.oracle_maxpool_backward.restype = ctypes.c_int
         self.lib = lib
 
     def threads(self) -> int:
@@ -111,6 +120,36 @@ class Oracle:
         return dict(M=d.M, nnz=d.nnz, d_max=d.d_max, n_empty=d.n_empty, dbar=d.dbar, cv=d.cv)
 
 
+    def transpose(self, rowptr, col, val, K, scale_mean=False):
+        """A^T in CSR: (rowptrT [K+1], colT [nnz], valT [nnz] or None)."""
+        rowptr = np.ascontiguousarray(rowptr, dtype=np.int32)
+        col = np.ascontiguousarray(col, dtype=np.int32)
+        val = None if val is None else np.ascontiguousarray(val, dtype=np.float32)
+        M = len(rowptr) - 1
+        nnz = int(rowptr[-1])
+        rT = np.empty(K + 1, np.int32)
+        cT = np.empty(nnz, np.int32)
+        vT = np.empty(nnz, np.float32) if (val is not None or scale_mean) else None
+        if self.lib.oracle_transpose(M, K, _ptr(rowptr), _ptr(col), _ptr(val), int(scale_mean),
+                                     _ptr(rT), _ptr(cT), _ptr(vT)) != 0:
+            raise ValueError("oracle_transpose rejected its arguments")
+        return rT, cT, vT
+
+    def maxpool_backward(self, rowptr, col, val, argmax, dC, K):
+        """dB [K, N] of the max reduction, given the forward argmax and dC [M, N]."""
+        rowptr = np.ascontiguousarray(rowptr, dtype=np.int32)
+        col = np.ascontiguousarray(col, dtype=np.int32)
+        val = None if val is None else np.ascontiguousarray(val, dtype=np.float32)
+        argmax = np.ascontiguousarray(argmax, dtype=np.int32)
+        dC = np.ascontiguousarray(dC, dtype=np.float32)
+        M, N = dC.shape
+        dB = np.empty((K, N), np.float32)
+        if self.lib.oracle_maxpool_backward(M, K, N, _ptr(rowptr), _ptr(col), _ptr(val),
+                                            _ptr(argmax), _ptr(dC), _ptr(dB)) != 0:
+            raise ValueError("oracle_maxpool_backward rejected its arguments")
+        return dB
+
+
 def planted(n: int, out_dir: str) -> Oracle:
     """A build with planted mistake n (1..5), for the tests that check the pins."""
     out = os.path.join(out_dir, f"libspmm_oracle_plant{n}.so")
@@ -140,3 +179,13 @@ def spmm(rowptr, col, val, B, reduce: str, rows=None, K=None):
 def descriptors(rowptr) -> dict:
     """M, nnz, d_max, n_empty, dbar = nnz/M, cv = std(d)/mean(d) over all rows."""
     return _default().descriptors(rowptr)
+
+
+def transpose(rowptr, col, val, K, scale_mean=False):
+    """A^T in CSR (stable by row); scale_mean divides each value by its row's degree."""
+    return _default().transpose(rowptr, col, val, K, scale_mean)
+
+
+def maxpool_backward(rowptr, col, val, argmax, dC, K):
+    """Gradient of the max reduction with respect to B."""
+    return _default().maxpool_backward(rowptr, col, val, argmax, dC, K)

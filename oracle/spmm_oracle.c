@@ -219,3 +219,67 @@ int oracle_descriptors(int64_t M, const int32_t *rowptr, oracle_desc *out) {
     out->cv = (s1 == 0) ? 0.0 : sqrt(var > 0.0 ? var : 0.0) / out->dbar;
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Backward of the three reductions (graph-spmm card, "Requirements and
+ * limits": the backward of a sum aggregation is the transposed product,
+ * from a second adjacency on the reversed edge list; "Method"/"API": the
+ * argmax returned by spmm_max feeds the max-pool backward).
+ *
+ * oracle_transpose: A^T in CSR. Row j of A^T holds every stored entry (i, j)
+ * of A, in increasing i, and entries of one row i in their CSR order (a
+ * stable counting sort of the entries by column). With scale_mean, the value
+ * of entry (i, j) is a_ij / d_i rounded once (1 / d_i for an unweighted A):
+ * then A_mean^T . dC is the mean's backward.
+ *
+ * oracle_maxpool_backward: dB[j, k] = sum over rows i with argmax[i, k] == j
+ * and over the stored entries p of row i with col[p] == j of a_p * dC[i, k]
+ * (fp64, rounded once). A duplicated winning pair contributes once per copy.
+ * ------------------------------------------------------------------------ */
+int oracle_transpose(int64_t M, int64_t K, const int32_t *rowptr, const int32_t *col,
+                     const float *val, int scale_mean, int32_t *rowptrT, int32_t *colT,
+                     float *valT) {
+    if (M < 0 || K < 0 || !rowptr || !rowptrT) return -1;
+    const int64_t nnz = rowptr[M];
+    for (int64_t j = 0; j <= K; ++j) rowptrT[j] = 0;
+    for (int64_t p = 0; p < nnz; ++p) {
+        if (col[p] < 0 || col[p] >= K) return -1;
+        rowptrT[col[p] + 1] += 1;
+    }
+    for (int64_t j = 0; j < K; ++j) rowptrT[j + 1] += rowptrT[j];
+    int32_t *next = (int32_t *)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
+    if (!next) return -1;
+    for (int64_t j = 0; j < K; ++j) next[j] = rowptrT[j];
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t d = rowptr[i + 1] - rowptr[i];
+        for (int64_t p = rowptr[i]; p < rowptr[i + 1]; ++p) {
+            const int32_t q = next[col[p]]++;
+            colT[q] = (int32_t)i;
+            if (valT) {
+                const double a = val ? (double)val[p] : 1.0;
+                valT[q] = scale_mean ? (float)(a / (double)d) : (float)a;
+            }
+        }
+    }
+    free(next);
+    return 0;
+}
+
+int oracle_maxpool_backward(int64_t M, int64_t K, int64_t N, const int32_t *rowptr,
+                            const int32_t *col, const float *val, const int32_t *argmax,
+                            const float *dC, float *dB) {
+    if (M < 0 || K < 0 || N < 0 || !rowptr || !argmax || !dC || !dB) return -1;
+    double *acc = (double *)calloc((size_t)(K * N > 0 ? K * N : 1), sizeof(double));
+    if (!acc) return -1;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t p = rowptr[i]; p < rowptr[i + 1]; ++p) {
+            const int32_t j = col[p];
+            const double a = val ? (double)val[p] : 1.0;
+            for (int64_t k = 0; k < N; ++k)
+                if (argmax[i * N + k] == j) acc[(int64_t)j * N + k] += a * (double)dC[i * N + k];
+        }
+    }
+    for (int64_t q = 0; q < K * N; ++q) dB[q] = (float)acc[q];
+    free(acc);
+    return 0;
+}
