@@ -226,6 +226,54 @@ spmm_status spmm_run_noalloc(const int32_t *rowptr, const int32_t *col, const fl
                              const float *B, int64_t M, int64_t K, int64_t N, spmm_reduce reduce,
                              float *C, int32_t *argmax, void *stream);
 
+/*
+ * spmm_transpose -- A^T in CSR, for the backward of a product (graph-spmm
+ * model card, "Requirements and limits": the gradient of a sum aggregation
+ * with respect to B is the product with the transposed adjacency, A^T . dC).
+ *   plan    : the plan of A (M x K).
+ *   col     : device, int32 [nnz], every value in [0, K) (validated columns;
+ *             an out-of-range column gives an undefined result but no fault).
+ *   val     : device, fp32 [nnz], or NULL for an unweighted A.
+ *   scale_mean : nonzero -> the value of entry (i, j) becomes a_ij / d_i
+ *             (1 / d_i when val is NULL), computed in fp64 and rounded once to
+ *             fp32, d_i the stored-entry count of row i: then a product with
+ *             the result is the backward of the mean.
+ *   rowptrT : device, int32 [K + 1], written.
+ *   colT    : device, int32 [nnz], written: row j of A^T lists the rows i of
+ *             the entries (i, j) of A in increasing i, and the entries of one
+ *             row i in their CSR order (a stable sort of the entries by column).
+ *   valT    : device, fp32 [nnz], written (the entries' values in colT's
+ *             order), or NULL to skip the values. Required when val != NULL or
+ *             scale_mean; when val is NULL and valT is not, every value is 1
+ *             (or 1 / d_i).
+ * Each output element is a pure function of the input: the sort places every
+ * entry by exact integer ranks, with no atomics. Synchronous: temporaries of
+ * about 5 x 4 x nnz bytes are allocated with cudaMalloc and freed before the
+ * call returns. SPMM_ERR_OOM if they do not fit.
+ */
+spmm_status spmm_transpose(spmm_plan_t plan, const int32_t *col, const float *val, int scale_mean,
+                           int32_t *rowptrT, int32_t *colT, float *valT, void *stream);
+
+/*
+ * spmm_maxpool_backward -- the gradient of spmm_max with respect to B
+ * (graph-spmm model card, "API": spmm_max returns the argmax so that the
+ * max-pool backward can route the gradient to the winning column).
+ *   planT  : the plan of A^T (K x M), built from spmm_transpose's rowptrT.
+ *   colT, valT : spmm_transpose's output (valT unscaled, or NULL when A is
+ *            unweighted).
+ *   argmax : device, int32 [M, N], as written by spmm_run with SPMM_MAX.
+ *   dC     : device, fp32 [M, N], the gradient of C.
+ *   dB     : device, fp32 [K, N], written once per element:
+ *            dB[j, c] = sum over the entries (i, j) of A with argmax[i, c] == j
+ *            of a_ij * dC[i, c] (every stored copy of a duplicated pair counts),
+ *            accumulated in fp32 in increasing i; 0 where no row chose j.
+ * Asynchronous; no allocation. 128-bit loads when N % 4 == 0 and argmax, dC
+ * and dB are 16-byte aligned.
+ */
+spmm_status spmm_maxpool_backward(spmm_plan_t planT, const int32_t *colT, const float *valT,
+                                  const int32_t *argmax, const float *dC, int64_t N, float *dB,
+                                  void *stream);
+
 /* spmm_plan_destroy -- free the plan and everything it owns. NULL is a no-op. */
 spmm_status spmm_plan_destroy(spmm_plan_t plan);
 

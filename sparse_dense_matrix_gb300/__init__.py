@@ -30,7 +30,7 @@ __all__ = [
     "spmm_plan_create", "spmm_run", "spmm_plan_describe", "spmm_plan_destroy",
     "spmm_plan_reserve", "spmm_plan_validate_cols", "spmm_plan_sync", "spmm_plan_set_family",
     "spmm_route", "spmm_default_t_split", "spmm_status_string", "spmm_launch_count",
-    "spmm_run_noalloc",
+    "spmm_run_noalloc", "spmm_transpose", "spmm_maxpool_backward",
     "PlanInfo", "REDUCE", "FAMILY", "lib", "build_library",
 ]
 
@@ -91,6 +91,8 @@ def _load():
         "spmm_status_string": ([i32], ctypes.c_char_p),
         "spmm_launch_count": ([], ctypes.c_uint64),
         "spmm_run_noalloc": ([vp, vp, vp, vp, i64, i64, i64, i32, vp, vp, vp], i32),
+        "spmm_transpose": ([vp, vp, vp, i32, vp, vp, vp, vp], i32),
+        "spmm_maxpool_backward": ([vp, vp, vp, vp, vp, i64, vp, vp], i32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(L, name)
@@ -192,6 +194,20 @@ def spmm_run_noalloc(rowptr_ptr: int, col_ptr: int, val_ptr, B_ptr: int, M: int,
                                 argmax_ptr, _stream_handle(stream)), "spmm_run_noalloc")
 
 
+def spmm_transpose(plan: int, col_ptr, val_ptr, scale_mean: bool, rowptrT_ptr: int, colT_ptr,
+                   valT_ptr, stream=None) -> None:
+    """A^T in CSR (synchronous; see include/spmm.h)."""
+    _check(lib.spmm_transpose(plan, col_ptr, val_ptr, 1 if scale_mean else 0, rowptrT_ptr,
+                              colT_ptr, valT_ptr, _stream_handle(stream)), "spmm_transpose")
+
+
+def spmm_maxpool_backward(planT: int, colT_ptr, valT_ptr, argmax_ptr, dC_ptr, N: int, dB_ptr: int,
+                          stream=None) -> None:
+    """Gradient of spmm_max with respect to B, through the plan of A^T."""
+    _check(lib.spmm_maxpool_backward(planT, colT_ptr, valT_ptr, argmax_ptr, dC_ptr, N, dB_ptr,
+                                     _stream_handle(stream)), "spmm_maxpool_backward")
+
+
 # ------------------------------------------------------------ tensor API
 def _req(t, dtype, name, dev=None):
     import torch
@@ -228,6 +244,7 @@ class SparseAdj:
         self.K = int(num_cols) if num_cols is not None else self.M
         self.rowptr, self.col, self.val = rowptr, col, val
         self._plan = None
+        self._t = self._tmean = None
         with torch.cuda.device(dev):
             self._plan = spmm_plan_create(rowptr.data_ptr(), self.M, self.K)
             info = spmm_plan_describe(self._plan, 0, 0)
@@ -293,7 +310,66 @@ class SparseAdj:
     def __matmul__(self, mat):
         return self.reduce(mat, "sum")
 
+    def transpose(self, scale_mean: bool = False) -> "SparseAdj":
+        """A^T as a new SparseAdj (K x M). With ``scale_mean`` the value of entry
+        (i, j) is a_ij / d_i, so that ``adj.transpose(True) @ dC`` is the
+        gradient of ``adj.reduce(B, "mean")`` with respect to B."""
+        import torch
+        nnz = self.col.numel()
+        rowptrT = torch.empty(self.K + 1, dtype=torch.int32, device=self.device)
+        colT = torch.empty(nnz, dtype=torch.int32, device=self.device)
+        valT = (torch.empty(nnz, dtype=torch.float32, device=self.device)
+                if (self.val is not None or scale_mean) else None)
+        with torch.cuda.device(self.device):
+            spmm_transpose(self.plan, self.col.data_ptr(),
+                           None if self.val is None else self.val.data_ptr(), scale_mean,
+                           rowptrT.data_ptr(), colT.data_ptr(),
+                           None if valT is None else valT.data_ptr())
+        return SparseAdj(rowptrT, colT, valT, num_cols=self.M)
+
+    def maxpool_backward(self, argmax, grad, out=None, stream=None):
+        """Called on A^T (from ``transpose()``): the gradient of the max
+        reduction with respect to B, given its argmax [M, N] and dC [M, N]."""
+        import torch
+        _req(argmax, torch.int32, "argmax", self.device)
+        _req(grad, torch.float32, "grad", self.device)
+        if grad.dim() != 2 or grad.shape[0] != self.K or tuple(argmax.shape) != tuple(grad.shape):
+            raise ValueError("argmax and grad must both be [M, N] with M the rows of A")
+        N = grad.shape[1]
+        if out is None:
+            out = torch.empty((self.M, N), dtype=torch.float32, device=self.device)
+        else:
+            _req(out, torch.float32, "out", self.device)
+            if tuple(out.shape) != (self.M, N):
+                raise ValueError("out has the wrong shape")
+        with torch.cuda.device(self.device):
+            spmm_maxpool_backward(self.plan, self.col.data_ptr(),
+                                  None if self.val is None else self.val.data_ptr(),
+                                  argmax.data_ptr(), grad.data_ptr(), N, out.data_ptr(), stream)
+        return out
+
+    def backward(self, grad, reduce: str = "sum", argmax=None):
+        """Gradient with respect to B of ``self.reduce(B, reduce)`` given dC.
+        The transposes are built on first use and kept."""
+        if reduce not in REDUCE:
+            raise ValueError(f"unknown reduce {reduce!r}")
+        if reduce == "mean":
+            if self._tmean is None:
+                self._tmean = self.transpose(scale_mean=True)
+            return self._tmean.reduce(grad, "sum")
+        if self._t is None:
+            self._t = self.transpose()
+        if reduce == "sum":
+            return self._t.reduce(grad, "sum")
+        if argmax is None:
+            raise ValueError("the max backward needs the forward's argmax")
+        return self._t.maxpool_backward(argmax, grad)
+
     def close(self) -> None:
+        for t in (getattr(self, "_t", None), getattr(self, "_tmean", None)):
+            if t is not None:
+                t.close()
+        self._t = self._tmean = None
         if self._plan is not None:
             spmm_plan_destroy(self._plan)
             self._plan = None
