@@ -85,7 +85,8 @@ typedef struct {
     int32_t vec;            /* columns per lane load: 4 (128-bit) or 1               */
     int32_t lanes;          /* lanes that share one entry (one per vec of columns)   */
     int32_t rows_per_warp;  /* rows one warp owns (ROWGROUP), else 1                 */
-    int32_t col_tiles;      /* column tiles of 32*vec columns (grid dimension y)     */
+    int32_t col_tiles;      /* column tiles (grid dimension y): lanes*vec columns each, 
+                               WINDOW: 4*lanes*window_chunks columns each             */
     int32_t launches;       /* kernel launches one spmm_run makes                    */
     int32_t num_sms;        /* SM count the routing assumed                          */
     int64_t workspace_bytes;/* device scratch spmm_run needs for this (N, reduce)    */
@@ -96,6 +97,7 @@ typedef struct {
     int32_t window_rows;    /* WINDOW family: rows per tile (0 for other families)      */
     int32_t window_ctas;    /* WINDOW family: CTAs per column tile                      */
     int64_t window_smem;    /* WINDOW family: dynamic shared memory per CTA, bytes      */
+    int32_t window_chunks;  /* WINDOW family: 4-column chunks per lane (cw = 4 lanes x chunks) */
 } spmm_plan_info;
 
 /*

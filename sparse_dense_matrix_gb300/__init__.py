@@ -53,7 +53,7 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes", ctypes.c_int64),
         ("band_w", ctypes.c_int64), ("band_cover", ctypes.c_double),
         ("window_rows", ctypes.c_int32), ("window_ctas", ctypes.c_int32),
-        ("window_smem", ctypes.c_int64),
+        ("window_smem", ctypes.c_int64), ("window_chunks", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -58,7 +58,8 @@ struct WinShape {
     int cap;        // ring rows, >= S R + 2W
     int S;          // pipeline stages
     int ecap;       // col/val entries staged per pipeline stage
-    int cw;         // B columns held per ring row (4 * lanes)
+    int L, Q;       // lanes per row, 4-column chunks per lane
+    int cw;         // B columns held per ring row (4 * L * Q)
     int Rp;         // row-pointer slots per stage (R + 1 rounded up to 4)
     int tmap;       // 1: ring rows are a column slice, loaded by 2-D tensor copies
     int pow2;       // 1: cap is a power of two
@@ -228,9 +229,9 @@ cudaError_t launch_heavy(const RunArgs &a, int vec, int lanes, int reduce, bool 
                          int tiles, cudaStream_t s);
 cudaError_t launch_coltile(const RunArgs &a, int wpr, int tiles_y, int reduce, bool has_val,
                            bool bulk_ok, cudaStream_t s);
-cudaError_t launch_window(const RunArgs &a, const WinShape &w, int lanes, int reduce, bool has_val,
-                          bool check, int grid_x, int tiles, cudaStream_t s);
+cudaError_t launch_window(const RunArgs &a, const WinShape &w, int reduce, bool has_val, bool check,
+                          int grid_x, int tiles, cudaStream_t s);
 bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool has_val,
-                  int lanes, int rows_per_group, WinShape *out);
+                  int lanes, int chunks, int rows_per_group, WinShape *out);
 
 }  // namespace spmm

@@ -17,7 +17,7 @@ static void window_layout(WinShape &w, bool has_val, int S) {
     w.pow2 = 0;
     int off = 2 * kWinMaxStages * 8;
     w.off_meta = off;
-    off += kWinMaxStages * 16;
+    off += kWinMaxStages * kWinMetaInts * 4;
     off = (off + 15) & ~15;
     w.off_rp = off;
     off += S * w.Rp * 4;
@@ -32,15 +32,20 @@ static void window_layout(WinShape &w, bool has_val, int S) {
 }
 
 bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool has_val,
-                  int lanes, int rows_per_group, WinShape *o) {
+                  int lanes, int chunks, int rows_per_group, WinShape *o) {
     (void)M; (void)K;
-    if (lanes < 2 || lanes > 32 || W < 0 || N <= 0) return false;
+    // the (L, Q) shapes the kernel is instantiated for
+    const bool shape_ok = (lanes == 2 && chunks == 1) ||
+                          (chunks == 2 && (lanes == 2 || lanes == 4 || lanes == 8 || lanes == 16));
+    if (!shape_ok || W < 0 || N <= 0) return false;
     if (rows_per_group < 1 || rows_per_group > 2) return false;
     WinShape w{};
     // one or two rows per lane group (two keep more gathers in flight; one keeps
     // the staged entries of high-degree tiles within a stage)
+    w.L = lanes;
+    w.Q = chunks;
     w.R = rows_per_group * kWinConsumerWarps * kWarp / lanes;
-    w.cw = 4 * lanes;
+    w.cw = 4 * lanes * chunks;
     // a column slice of B comes by 2-D tensor copies of R-row boxes: W and cap
     // are then multiples of R so that boxes start on a multiple of R and never
     // wrap around the ring
@@ -101,18 +106,18 @@ cudaError_t encode_bmap(const RunArgs &a, const WinShape &w, CUtensorMap *map) {
 
 }  // namespace
 
-cudaError_t launch_window(const RunArgs &a, const WinShape &w, int lanes, int reduce, bool has_val,
-                          bool check, int grid_x, int tiles, cudaStream_t s) {
+cudaError_t launch_window(const RunArgs &a, const WinShape &w, int reduce, bool has_val, bool check,
+                          int grid_x, int tiles, cudaStream_t s) {
     CUtensorMap map;
     cudaError_t e = encode_bmap(a, w, &map);
     if (e != cudaSuccess) return e;
     switch (reduce) {
         case SPMM_SUM:
-            return launch_window_red<SPMM_SUM>(a, w, map, lanes, has_val, check, grid_x, tiles, s);
+            return launch_window_red<SPMM_SUM>(a, w, map, has_val, check, grid_x, tiles, s);
         case SPMM_MEAN:
-            return launch_window_red<SPMM_MEAN>(a, w, map, lanes, has_val, check, grid_x, tiles, s);
+            return launch_window_red<SPMM_MEAN>(a, w, map, has_val, check, grid_x, tiles, s);
         case SPMM_MAX:
-            return launch_window_red<SPMM_MAX>(a, w, map, lanes, has_val, check, grid_x, tiles, s);
+            return launch_window_red<SPMM_MAX>(a, w, map, has_val, check, grid_x, tiles, s);
     }
     return cudaErrorInvalidValue;
 }

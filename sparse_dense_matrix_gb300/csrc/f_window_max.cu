@@ -3,6 +3,6 @@
 
 namespace spmm {
 template cudaError_t launch_window_red<SPMM_MAX>(const RunArgs &, const WinShape &,
-                                              const CUtensorMap &, int, bool, bool, int, int,
+                                              const CUtensorMap &, bool, bool, int, int,
                                               cudaStream_t);
 }  // namespace spmm

@@ -358,6 +358,7 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     o->window_rows = 0;
     o->window_ctas = 0;
     o->window_smem = 0;
+    o->window_chunks = 0;
     o->vec = ((aligned & 1) && N % 4 == 0) ? 4 : 1;
     const int64_t n_vec = (N + o->vec - 1) / o->vec;
     int64_t lanes = std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil(n_vec)));
@@ -368,20 +369,25 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     const bool window_ok = (family_override == SPMM_FAMILY_AUTO || forced) &&
                            d->band_w > 0 && (aligned & 3) == 3 && N > 0 && N % 4 == 0 &&
                            (forced || (d->dbar >= 2.0 && d->band_cover >= 0.97)) && d->M > 0;
+    int64_t win_tiles = 0;
     if (window_ok) {
         bool found = false;
-        for (int64_t L = std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil((N + 3) / 4)));
-             L >= 2 && !found; L >>= 1) {
+        // column tiles of cw = 4 L Q columns, widest first: Q = 2 chunks per lane
+        // (L = cw / 8) down to cw = 16, then L = 2, Q = 1 for cw = 8
+        for (int64_t cw = 4 * std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil((N + 3) / 4)));
+             cw >= 8 && !found; cw >>= 1) {
+            const int L = cw == 8 ? 2 : (int)(cw / 8);
+            const int Q = cw == 8 ? 1 : 2;
             for (int rpg = 2; rpg >= 1 && !found; --rpg) {
                 WinShape w;
-                if (!window_shape(d->M, d->K, N, d->dbar, d->band_w, !(aligned & 4), (int)L, rpg,
+                if (!window_shape(d->M, d->K, N, d->dbar, d->band_w, !(aligned & 4), L, Q, rpg,
                                   &w))
                     continue;
                 if (w.smem_bytes > kWindowSmemBudget) continue;
                 // the staged entries of an average tile must fit a stage (else the
                 // tile is read from global memory)
                 if (!forced && (double)w.R * d->dbar * 1.25 + 64 > (double)w.ecap) continue;
-                const int64_t tiles_y = (N + 4 * L - 1) / (4 * L);
+                const int64_t tiles_y = (N + cw - 1) / cw;
                 if (!forced && tiles_y > 4) continue;
                 const int64_t ctas = std::max<int64_t>(
                     1, (num_sms > 0 ? num_sms : 1) * w.ctas_per_sm / tiles_y);
@@ -390,6 +396,8 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
                 if (!forced && 2 * d->band_w > 2 * (d->M / ctas)) continue;
                 fam = SPMM_FAMILY_WINDOW;
                 lanes = L;
+                win_tiles = tiles_y;
+                o->window_chunks = Q;
                 o->window_rows = w.R;
                 o->window_ctas = (int32_t)ctas;
                 o->window_smem = w.smem_bytes;
@@ -413,7 +421,9 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     }
     if (fam == SPMM_FAMILY_COLTILE) lanes = 32;     // one 128-column tile per warp
     o->lanes = (int32_t)lanes;
-    o->col_tiles = (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
+    o->col_tiles = fam == SPMM_FAMILY_WINDOW
+                       ? (int32_t)win_tiles
+                       : (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
     o->family = fam;
     o->rows_per_warp = fam == SPMM_FAMILY_ROWGROUP ? (int32_t)(32 / lanes) : 1;
     o->launches = (d->M > 0 && N > 0) ? 1 + (d->n_heavy > 0 ? 2 : 0) : 0;
@@ -676,8 +686,9 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
     if (r.family == SPMM_FAMILY_WINDOW) {
         WinShape w;
         const int rpg = (int)((int64_t)r.window_rows * r.lanes / (kWarp * 16));
-        window_shape(p->M, p->K, N, p->dbar, p->band_w, has_val, r.lanes, rpg, &w);
-        e = launch_window(a, w, r.lanes, reduce, has_val, !p->band_all, r.window_ctas,
+        window_shape(p->M, p->K, N, p->dbar, p->band_w, has_val, r.lanes, r.window_chunks, rpg,
+                     &w);
+        e = launch_window(a, w, reduce, has_val, !p->band_all, r.window_ctas,
                           r.col_tiles, s);
     } else if (r.family == SPMM_FAMILY_COLTILE) {
         // warps per row: the column tiles, up to a CTA's 8 warps (a power of two)
@@ -690,8 +701,16 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
         e = launch_rowgroup(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
     else
         e = launch_warprow(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
-    if (e == cudaSuccess && p->n_heavy > 0)
-        e = launch_heavy(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
+    if (e == cudaSuccess && p->n_heavy > 0) {
+        // the split rows take the lane shape of the row-per-warp families (the
+        // WINDOW family's lanes cover only part of its column tile)
+        int64_t hl = r.lanes, ht = r.col_tiles;
+        if (r.family == SPMM_FAMILY_WINDOW) {
+            hl = std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil(a.n_vec)));
+            ht = (a.n_vec + hl - 1) / hl;
+        }
+        e = launch_heavy(a, r.vec, (int)hl, reduce, has_val, (int)ht, s);
+    }
     return from_cuda(e);
 }
 

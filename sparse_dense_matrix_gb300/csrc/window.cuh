@@ -13,11 +13,18 @@
 //     rows of the tiles still in flight are never overwritten). Whole rows (cw == N) come by 1-D bulk
 //     copies; a column slice (cw < N) comes by 2-D tensor copies of R x cw
 //     boxes, with W and cap multiples of R so that boxes never wrap.
-// Sixteen consumer warps (L lanes per row, two rows per lane group) read the
-// entries from shared memory and the gathered B rows from the ring; an entry
-// outside the window (possible only when not every entry is within W) is read
-// from global memory instead. Every B row is thus fetched from L2/HBM once per
-// CTA range (plus a 2W halo) rather than once per entry.
+// The producer also writes, per stage, the constants the consumers need for
+// the tile (shared addresses of the staged entries, window bounds, ring base).
+// Sixteen consumer warps read the entries from shared memory and the gathered
+// B rows from the ring. L lanes share a row; each lane owns Q chunks of four
+// columns (cw = 4 L Q). With Q = 2, lane groups of even and odd index read
+// their two chunks in opposite order, so the two groups that share a
+// quarter-warp phase of a 128-bit load touch disjoint halves of their ring
+// rows (no bank conflicts when a ring row is 128 bytes), and one slot
+// computation serves two 16-byte gathers. An entry outside the window
+// (possible only when not every entry is within W) is read from global memory
+// instead. Every B row is thus fetched from L2/HBM once per CTA range (plus a
+// 2W halo) rather than once per entry.
 // Rows longer than t_split are left to the heavy-row split, as everywhere.
 // Per lane the entries are accumulated in CSR order with fp32 FMA.
 #pragma once
@@ -30,8 +37,121 @@ namespace spmm {
 constexpr int kWinMaxStages = 8;
 constexpr int kWinConsumerWarps = 16;
 constexpr int kWinThreads = (kWinConsumerWarps + 1) * kWarp;
+constexpr int kWinMetaInts = 8;   // per-stage constants, see k_window
 
-template <int L, int RED, bool HAS_VAL, bool CHECK, bool POW2>
+// shared loads at a compile-time byte offset from a 32-bit shared address
+template <int OFF>
+__device__ __forceinline__ int lds_s32_at(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF));
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ float lds_f32_at(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(addr), "n"(OFF));
+    return v;
+}
+
+// Consumer-side state of one tile and the gathers of a lane.
+template <int L, int Q, int RED, bool HAS_VAL, bool CHECK, bool POW2>
+struct WinLane {
+    using A = Acc<4, RED, HAS_VAL>;
+    static constexpr uint32_t kRowBytes = 16u * L * Q;
+    uint32_t ring_k[Q];        // shared address of this lane's k-th chunk in ring row 0
+    const float *Bg[Q];        // global fallback for out-of-window entries
+    int64_t N;
+    uint32_t mask, cap;        // ring size (mask = cap - 1 when it is a power of two)
+    int win_lo, base;          // tile window start; ring slot of row j = j - base (mod cap)
+    unsigned win_span;
+
+    __device__ __forceinline__ void fetch(int j, float (&b)[Q][4]) const {
+        if (!CHECK || (unsigned)(j - win_lo) < win_span) {
+            uint32_t slot;
+            if constexpr (POW2) {
+                slot = (uint32_t)j & mask;
+            } else {
+                const uint32_t s0 = (uint32_t)(j - base);   // in [0, 2 cap)
+                slot = min(s0, s0 - cap);                   // s0 or s0 - cap
+            }
+            const uint32_t ro = slot * kRowBytes;
+#pragma unroll
+            for (int k = 0; k < Q; ++k) lds_v4(ring_k[k] + ro, b[k]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < Q; ++k) ld_vec<4>(Bg[k] + (int64_t)j * N, b[k]);
+        }
+    }
+
+    template <int NB, int U = 0>
+    __device__ __forceinline__ void load_entries(int (&j)[NB], float (&w)[NB], uint32_t ca,
+                                                 uint32_t va) const {
+        if constexpr (U < NB) {
+            j[U] = lds_s32_at<4 * U>(ca);
+            w[U] = HAS_VAL ? lds_f32_at<4 * U>(va) : 1.0f;
+            load_entries<NB, U + 1>(j, w, ca, va);
+        }
+    }
+
+    // NB consecutive entries of one row, all gathers in flight together
+    template <int NB>
+    __device__ __forceinline__ void run(A (&acc)[Q], uint32_t ca, uint32_t va) const {
+        int j[NB];
+        float w[NB], b[NB][Q][4];
+        load_entries<NB>(j, w, ca, va);
+#pragma unroll
+        for (int u = 0; u < NB; ++u) fetch(j[u], b[u]);
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+#pragma unroll
+            for (int k = 0; k < Q; ++k) acc[k].add(w[u], j[u], b[u][k]);
+    }
+
+    // NB entries of each of two rows, all gathers in flight together
+    template <int NB>
+    __device__ __forceinline__ void run2(A (&aa)[Q], uint32_t ca, uint32_t va, A (&ab)[Q],
+                                         uint32_t cb, uint32_t vb) const {
+        int j[2 * NB];
+        float w[2 * NB], b[2 * NB][Q][4];
+        int (&ja)[NB] = *reinterpret_cast<int (*)[NB]>(&j[0]);
+        int (&jb)[NB] = *reinterpret_cast<int (*)[NB]>(&j[NB]);
+        float (&wa)[NB] = *reinterpret_cast<float (*)[NB]>(&w[0]);
+        float (&wb)[NB] = *reinterpret_cast<float (*)[NB]>(&w[NB]);
+        load_entries<NB>(ja, wa, ca, va);
+        load_entries<NB>(jb, wb, cb, vb);
+#pragma unroll
+        for (int u = 0; u < 2 * NB; ++u) fetch(j[u], b[u]);
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+#pragma unroll
+            for (int k = 0; k < Q; ++k) aa[k].add(w[u], j[u], b[u][k]);
+#pragma unroll
+        for (int u = NB; u < 2 * NB; ++u)
+#pragma unroll
+            for (int k = 0; k < Q; ++k) ab[k].add(w[u], j[u], b[u][k]);
+    }
+
+    // the n entries of one row: batches of 8 / Q gathered rows (8 16-byte
+    // gathers in flight per lane), then 4, 2 and 1
+    __device__ __forceinline__ void run_row(A (&acc)[Q], uint32_t ca, uint32_t va, int n) const {
+        if constexpr (Q == 1) {
+            for (; n >= 8; n -= 8, ca += 32, va += 32) run<8>(acc, ca, va);
+            if (n >= 4) {
+                run<4>(acc, ca, va);
+                n -= 4; ca += 16; va += 16;
+            }
+        } else {
+            for (; n >= 4; n -= 4, ca += 16, va += 16) run<4>(acc, ca, va);
+        }
+        if (n >= 2) {
+            run<2>(acc, ca, va);
+            n -= 2; ca += 8; va += 8;
+        }
+        if (n) run<1>(acc, ca, va);
+    }
+};
+
+template <int L, int Q, int RED, bool HAS_VAL, bool CHECK, bool POW2>
 __global__ void __launch_bounds__(kWinThreads, 1)
     k_window(const RunArgs a, const WinShape w, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -40,7 +160,7 @@ __global__ void __launch_bounds__(kWinThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kWinMaxStages;
     const int S = w.S;
-    int *meta = reinterpret_cast<int *>(smem + w.off_meta);      // [S][4]
+    int *meta = reinterpret_cast<int *>(smem + w.off_meta);      // [S][kWinMetaInts]
     int *rp = reinterpret_cast<int *>(smem + w.off_rp);          // [S][Rp]
     int *scol = reinterpret_cast<int *>(smem + w.off_col);       // [S][ecap]
     float *sval = reinterpret_cast<float *>(smem + w.off_val);   // [S][ecap]
@@ -65,29 +185,37 @@ __global__ void __launch_bounds__(kWinThreads, 1)
 
     const int warp = threadIdx.x / kWarp;
     const int lane = threadIdx.x & (kWarp - 1);
-
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // Integer work here is incremental (no division in the loop): this warp
+        // shares its scheduler with four consumer warps, and a tile's copies
+        // must be issued well before the consumers reach it.
+        const int64_t R = w.R, W = w.W;
+        const int64_t Kr = (a.K + R - 1) / R * R;   // B rows rounded up to whole boxes
+        const uint32_t cap = (uint32_t)w.cap;
         int64_t loaded_hi = 0;   // B rows below loaded_hi have been requested
+        uint32_t hi_slot = 0;    // ring slot of row loaded_hi (loaded_hi mod cap)
+        int64_t prev_lo = 0;     // window start of the previous tile
+        uint32_t lo_mod = 0;     // prev_lo mod cap
         int issued = 0;
         // Segment bounds: lane l holds rowptr[start of tile kb + l] for the current
         // batch of 32 tiles (bcur) and the next batch (bnxt); a batch is loaded 32
         // tiles before it is used, so no tile waits on a row-pointer load.
         auto tile_start = [&](int kk) {
-            const int64_t q = min((t_begin + kk) * (int64_t)w.R, a.M);
+            const int64_t q = min((t_begin + kk) * R, a.M);
             return ld_stream(a.rowptr + q);
         };
         int bcur = tile_start(min(lane, n_tiles));
         int bnxt = tile_start(min(kWarp + lane, n_tiles));
-        for (int k = 0; k < n_tiles; ++k) {
-            const int s = k % S;
-            const uint32_t use = (uint32_t)(k / S);
-            if (use > 0) {
-                const bool ok = mbar_wait(&empty[s], (use - 1) & 1, a.err);
+        int s = 0;
+        uint32_t round = 0;      // k / S
+        int64_t r0 = t_begin * R;
+        for (int k = 0; k < n_tiles; ++k, r0 += R) {
+            if (round > 0) {
+                const bool ok = mbar_wait(&empty[s], (round - 1) & 1, a.err);
                 if (!__all_sync(0xffffffffu, ok)) break;
             }
-            const int64_t r0 = (t_begin + k) * w.R;
-            const int64_t r1 = min(r0 + w.R, a.M);
+            const int64_t r1 = min(r0 + R, a.M);
             const int kl = k & (kWarp - 1);
             if (kl == 0 && k > 0) {
                 bcur = bnxt;
@@ -97,6 +225,8 @@ __global__ void __launch_bounds__(kWinThreads, 1)
             const int seg_e = kl == kWarp - 1 ? __shfl_sync(0xffffffffu, bnxt, 0)
                                                : __shfl_sync(0xffffffffu, bcur, kl + 1);
             int *rps = rp + s * w.Rp;
+            int *scs = scol + s * w.ecap;
+            float *svs = sval + s * w.ecap;
             const int s_al = seg_b & ~3;
             const bool overflow = (seg_e - s_al) > w.ecap;
             int e_cp = s_al;                 // entries [s_al, e_cp) arrive by bulk copy
@@ -104,28 +234,44 @@ __global__ void __launch_bounds__(kWinThreads, 1)
                 e_cp = max(s_al, min((seg_e + 3) & ~3, a.nnz4));
                 // the last < 4 entries of the whole array: plain loads
                 for (int p = e_cp + lane; p < seg_e; p += kWarp) {
-                    scol[s * w.ecap + (p - s_al)] = ld_stream(a.col + p);
-                    if (HAS_VAL) sval[s * w.ecap + (p - s_al)] = ld_stream(a.val + p);
+                    scs[p - s_al] = ld_stream(a.col + p);
+                    if (HAS_VAL) svs[p - s_al] = ld_stream(a.val + p);
                 }
             }
-            // window of this tile, and the B rows it adds to the ring
-            const int64_t win_lo = max(r0 - (int64_t)w.W, (int64_t)0);
-            const int64_t win_hi = min(r1 + (int64_t)w.W, a.K);
-            int64_t lo = (k == 0) ? win_lo : max(loaded_hi, win_lo);
-            int64_t hi = max(win_hi, lo);
-            uint32_t ring_bytes;
-            if (w.tmap) {                    // whole R-row boxes (multiples of R)
-                hi = min((hi + w.R - 1) / w.R * w.R, (a.K + w.R - 1) / w.R * w.R);
-                hi = max(hi, lo);
-                ring_bytes = (uint32_t)((hi - lo) / w.R) * (uint32_t)w.R * (uint32_t)w.cw * 4u;
+            // window of this tile (empty when it lies past the last B row)
+            const int64_t win_lo = max(r0 - W, (int64_t)0);
+            const int64_t win_hi = max(min(r1 + W, a.K), win_lo);
+            if (k == 0) {
+                lo_mod = (uint32_t)(win_lo % cap);
             } else {
-                ring_bytes = (uint32_t)(hi - lo) * (uint32_t)cw_eff * 4u;
+                lo_mod += (uint32_t)(win_lo - prev_lo);   // advances by at most R <= cap
+                if (lo_mod >= cap) lo_mod -= cap;
             }
+            prev_lo = win_lo;
+            // the B rows this tile adds to the ring: [lo, hi), contiguous with
+            // what is loaded (the window only moves forward)
+            int64_t lo = win_lo, hi;
+            uint32_t lo_slot = lo_mod;
+            if (k > 0 && loaded_hi >= win_lo) {
+                lo = loaded_hi;
+                lo_slot = hi_slot;
+            }
+            // whole R-row boxes when the ring holds a column slice: W and the
+            // tile starts are multiples of R, so r0 + R + W is one
+            hi = w.tmap ? min(r0 + R + W, Kr) : win_hi;
+            hi = max(hi, lo);
+            const uint32_t n_new = (uint32_t)(hi - lo);   // <= R + 2W <= cap
+            const uint32_t ring_bytes = n_new * (uint32_t)(w.tmap ? w.cw : cw_eff) * 4u;
             if (lane == 0) {
-                meta[4 * s + 0] = s_al;
-                meta[4 * s + 1] = overflow ? 1 : 0;
-                meta[4 * s + 2] = (int)win_lo;
-                meta[4 * s + 3] = (int)win_hi;
+                // constants of the tile for the consumers (published by the
+                // arrive below, which orders these stores before the phase flip)
+                int *m = meta + kWinMetaInts * s;
+                m[0] = (int)(smem_addr(scs) - 4u * (uint32_t)s_al);
+                m[1] = (int)(smem_addr(svs) - 4u * (uint32_t)s_al);
+                m[2] = overflow ? 1 : 0;
+                m[3] = (int)win_lo;
+                m[4] = (int)(win_hi - win_lo);
+                m[5] = (int)(win_lo - (int64_t)lo_mod);
             }
             const uint32_t seg_bytes = (uint32_t)(e_cp - s_al) * 4u;
             const uint32_t rp_bytes = (uint32_t)w.Rp * 4u;
@@ -136,31 +282,47 @@ __global__ void __launch_bounds__(kWinThreads, 1)
             // row pointers of the tile: the plan's copy is padded past rowptr[M]
             if (lane == 3) bulk_g2s(rps, a.rowptr + r0, rp_bytes, &full[s]);
             if (seg_bytes) {
-                if (lane == 0) bulk_g2s(scol + s * w.ecap, a.col + s_al, seg_bytes, &full[s]);
-                if (HAS_VAL && lane == 1) bulk_g2s(sval + s * w.ecap, a.val + s_al, seg_bytes, &full[s]);
+                if (lane == 0) bulk_g2s(scs, a.col + s_al, seg_bytes, &full[s]);
+                if (HAS_VAL && lane == 1) bulk_g2s(svs, a.val + s_al, seg_bytes, &full[s]);
             }
             if (w.tmap) {
-                for (int64_t y = lo + (int64_t)lane * w.R; y < hi; y += (int64_t)kWarp * w.R)
-                    tensor2d_g2s(ring + (y % w.cap) * w.cw, &bmap, col0, (int)y, &full[s]);
+                // boxes of R rows start on multiples of R and never wrap (cap is one)
+                for (uint32_t d = (uint32_t)lane * (uint32_t)R; d < n_new; d += kWarp * (uint32_t)R) {
+                    uint32_t slot = lo_slot + d;
+                    if (slot >= cap) slot -= cap;
+                    tensor2d_g2s(ring + (size_t)slot * w.cw, &bmap, col0, (int)(lo + d), &full[s]);
+                }
             } else if (w.cw == a.N) {
                 // ring rows are whole B rows: one copy per run up to the ring's wrap
                 if (lane == 2) {
-                    int64_t j = lo;
-                    while (j < hi) {
-                        const int slot = (int)(j % w.cap);
-                        const int64_t run = min(hi - j, (int64_t)(w.cap - slot));
-                        bulk_g2s(ring + (int64_t)slot * w.cw, a.B + j * N,
-                                 (uint32_t)(run * N * 4), &full[s]);
-                        j += run;
+                    uint32_t d = 0, slot = lo_slot;
+                    while (d < n_new) {
+                        const uint32_t run = min(n_new - d, cap - slot);
+                        bulk_g2s(ring + (size_t)slot * w.cw, a.B + (lo + d) * N,
+                                 run * (uint32_t)N * 4u, &full[s]);
+                        d += run;
+                        slot += run;
+                        if (slot >= cap) slot -= cap;
                     }
                 }
             } else {
-                for (int64_t j = lo + lane; j < hi; j += kWarp)
-                    bulk_g2s(ring + (j % w.cap) * w.cw, a.B + j * N + col0,
+                for (uint32_t d = (uint32_t)lane; d < n_new; d += kWarp) {
+                    uint32_t slot = lo_slot + d;
+                    if (slot >= cap) slot -= cap;
+                    bulk_g2s(ring + (size_t)slot * w.cw, a.B + (lo + d) * N + col0,
                              (uint32_t)cw_eff * 4u, &full[s]);
+                }
             }
-            loaded_hi = max(loaded_hi, hi);
+            if (hi > loaded_hi || k == 0) {
+                loaded_hi = hi;
+                hi_slot = lo_slot + n_new;
+                if (hi_slot >= cap) hi_slot -= cap;
+            }
             issued = k + 1;
+            if (++s == S) {
+                s = 0;
+                ++round;
+            }
         }
         // never leave while copies this warp issued may still be landing
         for (int k = max(0, issued - S); k < issued; ++k)
@@ -169,96 +331,56 @@ __global__ void __launch_bounds__(kWinThreads, 1)
     }
 
     // -------------------------------------------------------------- consumers
+    using Lane = WinLane<L, Q, RED, HAS_VAL, CHECK, POW2>;
+    using A = typename Lane::A;
     constexpr int kGroups = kWinConsumerWarps * kWarp / L;
     const int ct = threadIdx.x - kWarp;
     const int grp = ct / L;
     const int li = ct % L;
-    const int c = col0 + 4 * li;               // first of this lane's 4 columns
-    const bool active = c < a.N;
-    const float *Bg = a.B + min(c, a.N - 4);   // global fallback (clamped for idle lanes)
-    constexpr int kRowBytes = 16 * L;          // one ring row: cw = 4L floats
-    const uint32_t ring_a = smem_addr(ring) + 16u * (uint32_t)li;
-    const int cap = w.cap;
-    const int mask = cap - 1;
-    for (int k = 0; k < n_tiles; ++k) {
-        const int s = k % S;
-        const bool ok = mbar_wait(&full[s], (uint32_t)(k / S) & 1, a.err);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const int64_t r0 = (t_begin + k) * w.R;
-        const int nr = (int)(min(r0 + w.R, a.M) - r0);
-        const int s_al = meta[4 * s + 0];
-        const bool overflow = meta[4 * s + 1] != 0;
-        const int win_lo = meta[4 * s + 2];
-        const unsigned win_span = (unsigned)(meta[4 * s + 3] - win_lo);
-        const int base = win_lo - win_lo % cap;    // slot(j) = j - base, minus cap if >= cap
-        const int *rps = rp + s * w.Rp;
-        // shared addresses of entry p: col at cs_a + 4p, val at vs_a + 4p
-        const uint32_t cs_a = smem_addr(scol + s * w.ecap) - 4u * (uint32_t)s_al;
-        const uint32_t vs_a = smem_addr(sval + s * w.ecap) - 4u * (uint32_t)s_al;
+    const int rot = Q > 1 ? grp % Q : 0;
+    Lane ln;
+    int cq[Q];                                   // first column of each chunk
+    bool act[Q];
+#pragma unroll
+    for (int k = 0; k < Q; ++k) {
+        const int chunk = li + L * ((k + rot) % Q);
+        ln.ring_k[k] = smem_addr(ring) + 16u * (uint32_t)chunk;
+        cq[k] = col0 + 4 * chunk;
+        act[k] = cq[k] < a.N;
+        ln.Bg[k] = a.B + min(cq[k], a.N - 4);    // clamped for idle lanes
+    }
+    ln.N = N;
+    ln.cap = (uint32_t)w.cap;
+    ln.mask = (uint32_t)w.cap - 1u;
 
-        auto fetch = [&](int j, float (&b)[4]) {
-            if (!CHECK || (unsigned)(j - win_lo) < win_span) {
-                int slot;
-                if constexpr (POW2) {
-                    slot = j & mask;
-                } else {
-                    slot = j - base;
-                    if (slot >= cap) slot -= cap;
-                }
-                lds_v4(ring_a + (uint32_t)slot * kRowBytes, b);
-            } else {
-                ld_vec<4>(Bg + (int64_t)j * N, b);
-            }
-        };
-
-        // Entries of one row from the staged segment: batches of 8 independent
-        // shared-memory gathers, then 4, then single entries.
-        auto run_row = [&](Acc<4, RED, HAS_VAL> &acc, uint32_t ca, uint32_t va, int n) {
-            for (; n >= 8; n -= 8, ca += 32, va += 32) {
-                int j[8];
-                float wv[8], b[8][4];
+    int64_t t_r0 = t_begin * w.R;               // first row of the current tile
+    auto store_row = [&](const A (&acc)[Q], int rr, int d) {
+        const int64_t i = t_r0 + rr;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    j[u] = lds_s32(ca + 4 * u);
-                    wv[u] = HAS_VAL ? lds_f32(va + 4 * u) : 1.0f;
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) fetch(j[u], b[u]);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) acc.add(wv[u], j[u], b[u]);
-            }
-            if (n >= 4) {
-                int j[4];
-                float wv[4], b[4][4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    j[u] = lds_s32(ca + 4 * u);
-                    wv[u] = HAS_VAL ? lds_f32(va + 4 * u) : 1.0f;
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) fetch(j[u], b[u]);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) acc.add(wv[u], j[u], b[u]);
-                n -= 4;
-                ca += 16;
-                va += 16;
-            }
-            for (; n > 0; --n, ca += 4, va += 4) {
-                const int j = lds_s32(ca);
-                float b[4];
-                fetch(j, b);
-                acc.add(HAS_VAL ? lds_f32(va) : 1.0f, j, b);
-            }
-        };
-        auto store_row = [&](const Acc<4, RED, HAS_VAL> &acc, int rr, int d) {
-            if (!active) return;
+        for (int k = 0; k < Q; ++k) {
+            if (!act[k]) continue;
             float out[4];
             int arg[4];
-            acc.finish(d, out, arg);
-            const int64_t i = r0 + rr;
-            st_vec<4>(a.C + i * N + c, out);
-            if (RED == SPMM_MAX && a.argmax) st_vec_i<4>(a.argmax + i * N + c, arg);
-        };
+            acc[k].finish(d, out, arg);
+            st_vec<4>(a.C + i * N + cq[k], out);
+            if (RED == SPMM_MAX && a.argmax) st_vec_i<4>(a.argmax + i * N + cq[k], arg);
+        }
+    };
+
+    int s = 0;
+    uint32_t phase = 0;
+    for (int k = 0; k < n_tiles; ++k, t_r0 += w.R) {
+        const bool ok = mbar_wait(&full[s], phase, a.err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const int nr = (int)(min(t_r0 + w.R, a.M) - t_r0);
+        const int *m = meta + kWinMetaInts * s;
+        const uint32_t cs_a = (uint32_t)m[0];   // shared address of entry p: cs_a + 4p
+        const uint32_t vs_a = (uint32_t)m[1];
+        const bool overflow = m[2] != 0;
+        ln.win_lo = m[3];
+        ln.win_span = (unsigned)m[4];
+        ln.base = m[5];
+        const int *rps = rp + s * w.Rp;
 
         // Each lane group takes rows grp and grp + kGroups together: two
         // independent entry streams interleaved four entries at a time.
@@ -269,42 +391,34 @@ __global__ void __launch_bounds__(kWinThreads, 1)
             const int pb = has_b ? rps[rb] : 0;
             const int db = has_b ? rps[rb + 1] - pb : 0;
             const bool do_a = da <= a.t_split, do_b = has_b && db <= a.t_split;
-            Acc<4, RED, HAS_VAL> acc_a, acc_b;
-            acc_a.init();
-            acc_b.init();
+            A acc_a[Q], acc_b[Q];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                acc_a[q].init();
+                acc_b[q].init();
+            }
             if (!overflow) {
                 uint32_t ca = cs_a + 4u * (uint32_t)pa, va = vs_a + 4u * (uint32_t)pa;
                 uint32_t cb = cs_a + 4u * (uint32_t)pb, vb = vs_a + 4u * (uint32_t)pb;
                 int na = do_a ? da : 0, nb = do_b ? db : 0;
-                for (; na >= 4 && nb >= 4; na -= 4, nb -= 4, ca += 16, va += 16, cb += 16, vb += 16) {
-                    int j[8];
-                    float wv[8], b[8][4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        j[u] = lds_s32(ca + 4 * u);
-                        j[4 + u] = lds_s32(cb + 4 * u);
-                        wv[u] = HAS_VAL ? lds_f32(va + 4 * u) : 1.0f;
-                        wv[4 + u] = HAS_VAL ? lds_f32(vb + 4 * u) : 1.0f;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) fetch(j[u], b[u]);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) acc_a.add(wv[u], j[u], b[u]);
-#pragma unroll
-                    for (int u = 4; u < 8; ++u) acc_b.add(wv[u], j[u], b[u]);
-                }
-                run_row(acc_a, ca, va, na);
-                run_row(acc_b, cb, vb, nb);
+                constexpr int kPair = 4 / Q;   // entries per row per step of the pair loop
+                for (; na >= kPair && nb >= kPair; na -= kPair, nb -= kPair, ca += 4 * kPair,
+                                                   va += 4 * kPair, cb += 4 * kPair, vb += 4 * kPair)
+                    ln.template run2<kPair>(acc_a, ca, va, acc_b, cb, vb);
+                ln.run_row(acc_a, ca, va, na);
+                if (nb) ln.run_row(acc_b, cb, vb, nb);
             } else {
                 for (int q = 0; q < 2; ++q) {
                     const int p0 = q ? pb : pa;
                     const int p1 = p0 + ((q ? do_b : do_a) ? (q ? db : da) : 0);
-                    Acc<4, RED, HAS_VAL> &acc = q ? acc_b : acc_a;
+                    A (&acc)[Q] = q ? acc_b : acc_a;
                     for (int p = p0; p < p1; ++p) {
                         const int j = ld_stream(a.col + p);
-                        float b[4];
-                        fetch(j, b);
-                        acc.add(HAS_VAL ? ld_stream(a.val + p) : 1.0f, j, b);
+                        const float wv = HAS_VAL ? ld_stream(a.val + p) : 1.0f;
+                        float b[Q][4];
+                        ln.fetch(j, b);
+#pragma unroll
+                        for (int kk = 0; kk < Q; ++kk) acc[kk].add(wv, j, b[kk]);
                     }
                 }
             }
@@ -313,15 +427,19 @@ __global__ void __launch_bounds__(kWinThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == S) {
+            s = 0;
+            phase ^= 1u;
+        }
     }
 }
 
 namespace window_detail {
-template <int L, int RED, bool HAS_VAL, bool CHECK>
+template <int L, int Q, int RED, bool HAS_VAL, bool CHECK>
 cudaError_t go(const RunArgs &a, const WinShape &w, const CUtensorMap &map, int grid_x, int tiles,
                cudaStream_t s) {
-    auto kern = w.pow2 ? k_window<L, RED, HAS_VAL, CHECK, true>
-                       : k_window<L, RED, HAS_VAL, CHECK, false>;
+    auto kern = w.pow2 ? k_window<L, Q, RED, HAS_VAL, CHECK, true>
+                       : k_window<L, Q, RED, HAS_VAL, CHECK, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          w.smem_bytes);
     if (e != cudaSuccess) return e;
@@ -330,27 +448,30 @@ cudaError_t go(const RunArgs &a, const WinShape &w, const CUtensorMap &map, int 
     return cudaGetLastError();
 }
 
+// (L, Q) shapes: column tiles of 8 (2 x 1), 16 (2 x 2), 32 (4 x 2), 64 (8 x 2)
+// and 128 (16 x 2) columns
 template <int RED, bool HAS_VAL, bool CHECK>
-cudaError_t by_lanes(const RunArgs &a, const WinShape &w, const CUtensorMap &map, int lanes,
-                     int gx, int tiles, cudaStream_t s) {
-    switch (lanes) {
-        case 2: return go<2, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
-        case 4: return go<4, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
-        case 8: return go<8, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
-        case 16: return go<16, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
-        case 32: return go<32, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
+cudaError_t by_lanes(const RunArgs &a, const WinShape &w, const CUtensorMap &map, int gx,
+                     int tiles, cudaStream_t s) {
+    const int key = w.L * 4 + w.Q;
+    switch (key) {
+        case 2 * 4 + 1: return go<2, 1, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
+        case 2 * 4 + 2: return go<2, 2, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
+        case 4 * 4 + 2: return go<4, 2, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
+        case 8 * 4 + 2: return go<8, 2, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
+        case 16 * 4 + 2: return go<16, 2, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 template <int RED>
-cudaError_t by_flags(const RunArgs &a, const WinShape &w, const CUtensorMap &map, int lanes,
-                     bool has_val, bool check, int gx, int tiles, cudaStream_t s) {
+cudaError_t by_flags(const RunArgs &a, const WinShape &w, const CUtensorMap &map, bool has_val,
+                     bool check, int gx, int tiles, cudaStream_t s) {
     if (has_val)
-        return check ? by_lanes<RED, true, true>(a, w, map, lanes, gx, tiles, s)
-                     : by_lanes<RED, true, false>(a, w, map, lanes, gx, tiles, s);
-    return check ? by_lanes<RED, false, true>(a, w, map, lanes, gx, tiles, s)
-                 : by_lanes<RED, false, false>(a, w, map, lanes, gx, tiles, s);
+        return check ? by_lanes<RED, true, true>(a, w, map, gx, tiles, s)
+                     : by_lanes<RED, true, false>(a, w, map, gx, tiles, s);
+    return check ? by_lanes<RED, false, true>(a, w, map, gx, tiles, s)
+                 : by_lanes<RED, false, false>(a, w, map, gx, tiles, s);
 }
 }  // namespace window_detail
 
@@ -358,19 +479,18 @@ cudaError_t by_flags(const RunArgs &a, const WinShape &w, const CUtensorMap &map
 // f_window_{sum,mean,max}.cu so that the variants compile in parallel).
 template <int RED>
 cudaError_t launch_window_red(const RunArgs &a, const WinShape &w, const CUtensorMap &map,
-                              int lanes, bool has_val, bool check, int gx, int tiles,
-                              cudaStream_t s) {
-    return window_detail::by_flags<RED>(a, w, map, lanes, has_val, check, gx, tiles, s);
+                              bool has_val, bool check, int gx, int tiles, cudaStream_t s) {
+    return window_detail::by_flags<RED>(a, w, map, has_val, check, gx, tiles, s);
 }
 
 extern template cudaError_t launch_window_red<SPMM_SUM>(const RunArgs &, const WinShape &,
-                                                        const CUtensorMap &, int, bool, bool,
-                                                        int, int, cudaStream_t);
+                                                        const CUtensorMap &, bool, bool, int,
+                                                        int, cudaStream_t);
 extern template cudaError_t launch_window_red<SPMM_MEAN>(const RunArgs &, const WinShape &,
-                                                         const CUtensorMap &, int, bool, bool,
-                                                         int, int, cudaStream_t);
+                                                         const CUtensorMap &, bool, bool, int,
+                                                         int, cudaStream_t);
 extern template cudaError_t launch_window_red<SPMM_MAX>(const RunArgs &, const WinShape &,
-                                                        const CUtensorMap &, int, bool, bool,
-                                                        int, int, cudaStream_t);
+                                                        const CUtensorMap &, bool, bool, int,
+                                                        int, cudaStream_t);
 
 }  // namespace spmm

@@ -136,15 +136,18 @@ def test_tensor_api_refuses_cpu_tensors(sdm):
 def test_router_window_rule(sdm):
     knn = dict(_desc(cv=0.0), band_w=512, band_cover=0.999)
     r = sdm.spmm_route(knn, 16, 0)
-    assert (r["family_name"], r["lanes"], r["col_tiles"], r["window_rows"]) == ("window", 4, 1, 256)
+    assert (r["family_name"], r["lanes"], r["window_chunks"], r["col_tiles"], r["window_rows"]) == \
+        ("window", 2, 2, 1, 256)
     assert 0 < r["window_smem"] <= 227 * 1024 and r["window_ctas"] == 152
     r = sdm.spmm_route(knn, 64, 1)
-    assert (r["family_name"], r["lanes"], r["col_tiles"], r["window_ctas"]) == ("window", 8, 2, 76)
+    assert (r["family_name"], r["lanes"], r["window_chunks"], r["col_tiles"], r["window_ctas"]) == \
+        ("window", 4, 2, 2, 76)
+    r = sdm.spmm_route(knn, 8, 0)
+    assert (r["family_name"], r["lanes"], r["window_chunks"], r["col_tiles"]) == ("window", 2, 1, 1)
     community = dict(_desc(M=65536, nnz=3668321, cv=0.1), band_w=256, band_cover=0.91)
     assert sdm.spmm_route(community, 128, 0)["family_name"] != "window"          # 9% outside W
-    dense_band = dict(community, band_cover=0.99)   # high degree: one row per lane group
-    r = sdm.spmm_route(dense_band, 128, 0)
-    assert (r["family_name"], r["lanes"], r["window_rows"]) == ("window", 16, 32)
+    dense_band = dict(community, band_cover=0.99)   # 56 entries per row: a tile overflows a stage
+    assert sdm.spmm_route(dense_band, 128, 0)["family_name"] != "window"
     assert sdm.spmm_route(dense_band, 512, 0)["family_name"] != "window"         # ring too big
     assert sdm.spmm_route(knn, 64, 0, aligned=1)["family_name"] == "rowgroup"   # col unaligned
     assert sdm.spmm_route(knn, 18, 0)["family_name"] != "window"                 # N % 4 != 0
