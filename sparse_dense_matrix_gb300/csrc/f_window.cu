@@ -35,7 +35,7 @@ bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool 
                   int lanes, int chunks, int rows_per_group, WinShape *o) {
     (void)M; (void)K;
     // the (L, Q) shapes the kernel is instantiated for
-    const bool shape_ok = (lanes == 2 && chunks == 1) ||
+    const bool shape_ok = (lanes == 2 && chunks == 1) || (lanes == 4 && chunks == 1) ||
                           (chunks == 2 && (lanes == 2 || lanes == 4 || lanes == 8 || lanes == 16));
     if (!shape_ok || W < 0 || N <= 0) return false;
     if (rows_per_group < 1 || rows_per_group > 2) return false;

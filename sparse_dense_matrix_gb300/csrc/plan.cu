@@ -376,8 +376,8 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
         // (L = cw / 8) down to cw = 16, then L = 2, Q = 1 for cw = 8
         for (int64_t cw = 4 * std::min<int64_t>(32, std::max<int64_t>(2, pow2ceil((N + 3) / 4)));
              cw >= 8 && !found; cw >>= 1) {
-            const int L = cw == 8 ? 2 : (int)(cw / 8);
-            const int Q = cw == 8 ? 1 : 2;
+            const int L = cw == 8 ? 2 : cw == 16 ? 4 : (int)(cw / 8);
+            const int Q = cw <= 16 ? 1 : 2;
             for (int rpg = 2; rpg >= 1 && !found; --rpg) {
                 WinShape w;
                 if (!window_shape(d->M, d->K, N, d->dbar, d->band_w, !(aligned & 4), L, Q, rpg,

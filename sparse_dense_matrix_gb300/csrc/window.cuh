@@ -187,141 +187,146 @@ __global__ void __launch_bounds__(kWinThreads, 1)
     const int lane = threadIdx.x & (kWarp - 1);
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // Integer work here is incremental (no division in the loop): this warp
-        // shares its scheduler with four consumer warps, and a tile's copies
-        // must be issued well before the consumers reach it.
+        // This warp shares its scheduler with four consumer warps and must issue
+        // a tile's copies well before the consumers reach it, so the per-tile
+        // bookkeeping is done 32 tiles at a time: lane l works out tile kb + l
+        // (segment bounds, window, the new ring rows and their slot), and the
+        // serial loop over the tiles only reads those values by shuffles.
         const int64_t R = w.R, W = w.W;
         const int64_t Kr = (a.K + R - 1) / R * R;   // B rows rounded up to whole boxes
         const uint32_t cap = (uint32_t)w.cap;
-        int64_t loaded_hi = 0;   // B rows below loaded_hi have been requested
-        uint32_t hi_slot = 0;    // ring slot of row loaded_hi (loaded_hi mod cap)
-        int64_t prev_lo = 0;     // window start of the previous tile
-        uint32_t lo_mod = 0;     // prev_lo mod cap
-        int issued = 0;
-        // Segment bounds: lane l holds rowptr[start of tile kb + l] for the current
-        // batch of 32 tiles (bcur) and the next batch (bnxt); a batch is loaded 32
-        // tiles before it is used, so no tile waits on a row-pointer load.
-        auto tile_start = [&](int kk) {
-            const int64_t q = min((t_begin + kk) * R, a.M);
-            return ld_stream(a.rowptr + q);
+        // row-pointer values of a batch, loaded one batch ahead
+        auto seg_load = [&](int kk, int &b, int &e) {
+            const int64_t q0 = min((t_begin + kk) * R, a.M);
+            b = ld_stream(a.rowptr + q0);
+            e = ld_stream(a.rowptr + min(q0 + R, a.M));
         };
-        int bcur = tile_start(min(lane, n_tiles));
-        int bnxt = tile_start(min(kWarp + lane, n_tiles));
+        int nb_b, nb_e;
+        seg_load(min(lane, n_tiles), nb_b, nb_e);
+        int64_t carry_hi = -1;   // highest B row requested before this batch (+1)
         int s = 0;
-        uint32_t round = 0;      // k / S
-        int64_t r0 = t_begin * R;
-        for (int k = 0; k < n_tiles; ++k, r0 += R) {
-            if (round > 0) {
-                const bool ok = mbar_wait(&empty[s], (round - 1) & 1, a.err);
-                if (!__all_sync(0xffffffffu, ok)) break;
-            }
+        uint32_t round = 0;      // tile / S
+        int issued = 0;
+        bool failed = false;
+        for (int kb = 0; kb < n_tiles && !failed; kb += kWarp) {
+            // ---- this lane's tile: kb + lane
+            const int kt = kb + lane;
+            const int seg_b = nb_b, seg_e = nb_e;
+            if (kb + kWarp < n_tiles) seg_load(min(kb + kWarp + lane, n_tiles), nb_b, nb_e);
+            const int64_t r0 = (t_begin + kt) * R;
             const int64_t r1 = min(r0 + R, a.M);
-            const int kl = k & (kWarp - 1);
-            if (kl == 0 && k > 0) {
-                bcur = bnxt;
-                bnxt = tile_start(min(k + kWarp + lane, n_tiles));
-            }
-            const int seg_b = __shfl_sync(0xffffffffu, bcur, kl);
-            const int seg_e = kl == kWarp - 1 ? __shfl_sync(0xffffffffu, bnxt, 0)
-                                               : __shfl_sync(0xffffffffu, bcur, kl + 1);
-            int *rps = rp + s * w.Rp;
-            int *scs = scol + s * w.ecap;
-            float *svs = sval + s * w.ecap;
             const int s_al = seg_b & ~3;
             const bool overflow = (seg_e - s_al) > w.ecap;
-            int e_cp = s_al;                 // entries [s_al, e_cp) arrive by bulk copy
-            if (!overflow) {
-                e_cp = max(s_al, min((seg_e + 3) & ~3, a.nnz4));
-                // the last < 4 entries of the whole array: plain loads
-                for (int p = e_cp + lane; p < seg_e; p += kWarp) {
-                    scs[p - s_al] = ld_stream(a.col + p);
-                    if (HAS_VAL) svs[p - s_al] = ld_stream(a.val + p);
-                }
-            }
-            // window of this tile (empty when it lies past the last B row)
+            const int e_cp = overflow ? s_al : max(s_al, min((seg_e + 3) & ~3, a.nnz4));
+            // window of the tile (empty when it lies past the last B row)
             const int64_t win_lo = max(r0 - W, (int64_t)0);
             const int64_t win_hi = max(min(r1 + W, a.K), win_lo);
-            if (k == 0) {
-                lo_mod = (uint32_t)(win_lo % cap);
-            } else {
-                lo_mod += (uint32_t)(win_lo - prev_lo);   // advances by at most R <= cap
-                if (lo_mod >= cap) lo_mod -= cap;
-            }
-            prev_lo = win_lo;
-            // the B rows this tile adds to the ring: [lo, hi), contiguous with
-            // what is loaded (the window only moves forward)
-            int64_t lo = win_lo, hi;
-            uint32_t lo_slot = lo_mod;
-            if (k > 0 && loaded_hi >= win_lo) {
-                lo = loaded_hi;
-                lo_slot = hi_slot;
-            }
-            // whole R-row boxes when the ring holds a column slice: W and the
-            // tile starts are multiples of R, so r0 + R + W is one
-            hi = w.tmap ? min(r0 + R + W, Kr) : win_hi;
-            hi = max(hi, lo);
-            const uint32_t n_new = (uint32_t)(hi - lo);   // <= R + 2W <= cap
-            const uint32_t ring_bytes = n_new * (uint32_t)(w.tmap ? w.cw : cw_eff) * 4u;
-            if (lane == 0) {
-                // constants of the tile for the consumers (published by the
-                // arrive below, which orders these stores before the phase flip)
-                int *m = meta + kWinMetaInts * s;
-                m[0] = (int)(smem_addr(scs) - 4u * (uint32_t)s_al);
-                m[1] = (int)(smem_addr(svs) - 4u * (uint32_t)s_al);
-                m[2] = overflow ? 1 : 0;
-                m[3] = (int)win_lo;
-                m[4] = (int)(win_hi - win_lo);
-                m[5] = (int)(win_lo - (int64_t)lo_mod);
-            }
-            const uint32_t seg_bytes = (uint32_t)(e_cp - s_al) * 4u;
-            const uint32_t rp_bytes = (uint32_t)w.Rp * 4u;
-            const uint32_t tx = rp_bytes + seg_bytes * (HAS_VAL ? 2u : 1u) + ring_bytes;
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], tx);
-            __syncwarp();
-            // row pointers of the tile: the plan's copy is padded past rowptr[M]
-            if (lane == 3) bulk_g2s(rps, a.rowptr + r0, rp_bytes, &full[s]);
-            if (seg_bytes) {
-                if (lane == 0) bulk_g2s(scs, a.col + s_al, seg_bytes, &full[s]);
-                if (HAS_VAL && lane == 1) bulk_g2s(svs, a.val + s_al, seg_bytes, &full[s]);
-            }
-            if (w.tmap) {
-                // boxes of R rows start on multiples of R and never wrap (cap is one)
-                for (uint32_t d = (uint32_t)lane * (uint32_t)R; d < n_new; d += kWarp * (uint32_t)R) {
-                    uint32_t slot = lo_slot + d;
-                    if (slot >= cap) slot -= cap;
-                    tensor2d_g2s(ring + (size_t)slot * w.cw, &bmap, col0, (int)(lo + d), &full[s]);
-                }
-            } else if (w.cw == a.N) {
-                // ring rows are whole B rows: one copy per run up to the ring's wrap
-                if (lane == 2) {
-                    uint32_t d = 0, slot = lo_slot;
-                    while (d < n_new) {
-                        const uint32_t run = min(n_new - d, cap - slot);
-                        bulk_g2s(ring + (size_t)slot * w.cw, a.B + (lo + d) * N,
-                                 run * (uint32_t)N * 4u, &full[s]);
-                        d += run;
-                        slot += run;
-                        if (slot >= cap) slot -= cap;
+            // rows requested through this tile: whole R-row boxes when the ring
+            // holds a column slice (W and the tile starts are multiples of R);
+            // non-decreasing in the tile index
+            const int64_t top = w.tmap ? min(r0 + R + W, Kr) : win_hi;
+            int64_t prev = __shfl_up_sync(0xffffffffu, top, 1);
+            if (lane == 0) prev = carry_hi;
+            carry_hi = __shfl_sync(0xffffffffu, top, kWarp - 1);
+            // new rows [lo, hi): contiguous with what is loaded
+            const int64_t lo = (prev >= win_lo) ? prev : win_lo;
+            const int64_t hi = max(top, lo);
+            const uint32_t lo_slot = (uint32_t)(lo % cap);
+            const uint32_t win_mod = (uint32_t)(win_lo % cap);
+            const int t_n_new = (int)(hi - lo);            // <= R + 2W <= cap
+            const int t_lo = (int)lo, t_win_lo = (int)win_lo, t_span = (int)(win_hi - win_lo);
+            const int t_base = (int)(win_lo - win_mod);
+
+            const int n_here = min(kWarp, n_tiles - kb);
+            for (int t = 0; t < n_here; ++t) {
+                const int k = kb + t;
+                if (round > 0) {
+                    const bool ok = mbar_wait(&empty[s], (round - 1) & 1, a.err);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        failed = true;
+                        break;
                     }
                 }
-            } else {
-                for (uint32_t d = (uint32_t)lane; d < n_new; d += kWarp) {
-                    uint32_t slot = lo_slot + d;
-                    if (slot >= cap) slot -= cap;
-                    bulk_g2s(ring + (size_t)slot * w.cw, a.B + (lo + d) * N + col0,
-                             (uint32_t)cw_eff * 4u, &full[s]);
+                const int c_sal = __shfl_sync(0xffffffffu, s_al, t);
+                const int c_ecp = __shfl_sync(0xffffffffu, e_cp, t);
+                const int c_sege = __shfl_sync(0xffffffffu, seg_e, t);
+                const bool c_over = __shfl_sync(0xffffffffu, overflow ? 1 : 0, t) != 0;
+                const int c_lo = __shfl_sync(0xffffffffu, t_lo, t);
+                const uint32_t c_slot = __shfl_sync(0xffffffffu, lo_slot, t);
+                const uint32_t c_new = (uint32_t)__shfl_sync(0xffffffffu, t_n_new, t);
+                const int64_t c_r0 = (t_begin + k) * R;
+                int *rps = rp + s * w.Rp;
+                int *scs = scol + s * w.ecap;
+                float *svs = sval + s * w.ecap;
+                // the last < 4 entries of the whole array: plain loads
+                if (!c_over) {
+                    for (int p = c_ecp + lane; p < c_sege; p += kWarp) {
+                        scs[p - c_sal] = ld_stream(a.col + p);
+                        if (HAS_VAL) svs[p - c_sal] = ld_stream(a.val + p);
+                    }
                 }
-            }
-            if (hi > loaded_hi || k == 0) {
-                loaded_hi = hi;
-                hi_slot = lo_slot + n_new;
-                if (hi_slot >= cap) hi_slot -= cap;
-            }
-            issued = k + 1;
-            if (++s == S) {
-                s = 0;
-                ++round;
+                const int c_wlo = __shfl_sync(0xffffffffu, t_win_lo, t);
+                const int c_span = __shfl_sync(0xffffffffu, t_span, t);
+                const int c_base = __shfl_sync(0xffffffffu, t_base, t);
+                if (lane == 0) {
+                    // constants of the tile for the consumers (published by the
+                    // arrive below, which orders these stores before the phase flip)
+                    int *m = meta + kWinMetaInts * s;
+                    m[0] = (int)(smem_addr(scs) - 4u * (uint32_t)c_sal);
+                    m[1] = (int)(smem_addr(svs) - 4u * (uint32_t)c_sal);
+                    m[2] = c_over ? 1 : 0;
+                    m[3] = c_wlo;
+                    m[4] = c_span;
+                    m[5] = c_base;
+                }
+                const uint32_t ring_bytes = c_new * (uint32_t)(w.tmap ? w.cw : cw_eff) * 4u;
+                const uint32_t seg_bytes = (uint32_t)(c_ecp - c_sal) * 4u;
+                const uint32_t rp_bytes = (uint32_t)w.Rp * 4u;
+                const uint32_t tx = rp_bytes + seg_bytes * (HAS_VAL ? 2u : 1u) + ring_bytes;
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], tx);
+                __syncwarp();
+                // row pointers of the tile: the plan's copy is padded past rowptr[M]
+                if (lane == 3) bulk_g2s(rps, a.rowptr + c_r0, rp_bytes, &full[s]);
+                if (seg_bytes) {
+                    if (lane == 0) bulk_g2s(scs, a.col + c_sal, seg_bytes, &full[s]);
+                    if (HAS_VAL && lane == 1) bulk_g2s(svs, a.val + c_sal, seg_bytes, &full[s]);
+                }
+                if (w.tmap) {
+                    // boxes of R rows start on multiples of R and never wrap (cap is one)
+                    for (uint32_t d = (uint32_t)lane * (uint32_t)R; d < c_new;
+                         d += kWarp * (uint32_t)R) {
+                        uint32_t slot = c_slot + d;
+                        if (slot >= cap) slot -= cap;
+                        tensor2d_g2s(ring + (size_t)slot * w.cw, &bmap, col0, c_lo + (int)d,
+                                     &full[s]);
+                    }
+                } else if (w.cw == a.N) {
+                    // ring rows are whole B rows: one copy per run up to the ring's wrap
+                    if (lane == 2) {
+                        uint32_t d = 0, slot = c_slot;
+                        while (d < c_new) {
+                            const uint32_t run = min(c_new - d, cap - slot);
+                            bulk_g2s(ring + (size_t)slot * w.cw, a.B + ((int64_t)c_lo + d) * N,
+                                     run * (uint32_t)N * 4u, &full[s]);
+                            d += run;
+                            slot += run;
+                            if (slot >= cap) slot -= cap;
+                        }
+                    }
+                } else {
+                    for (uint32_t d = (uint32_t)lane; d < c_new; d += kWarp) {
+                        uint32_t slot = c_slot + d;
+                        if (slot >= cap) slot -= cap;
+                        bulk_g2s(ring + (size_t)slot * w.cw, a.B + ((int64_t)c_lo + d) * N + col0,
+                                 (uint32_t)cw_eff * 4u, &full[s]);
+                    }
+                }
+                issued = k + 1;
+                if (++s == S) {
+                    s = 0;
+                    ++round;
+                }
             }
         }
         // never leave while copies this warp issued may still be landing
@@ -457,6 +462,7 @@ cudaError_t by_lanes(const RunArgs &a, const WinShape &w, const CUtensorMap &map
     switch (key) {
         case 2 * 4 + 1: return go<2, 1, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
         case 2 * 4 + 2: return go<2, 2, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
+        case 4 * 4 + 1: return go<4, 1, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
         case 4 * 4 + 2: return go<4, 2, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
         case 8 * 4 + 2: return go<8, 2, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
         case 16 * 4 + 2: return go<16, 2, RED, HAS_VAL, CHECK>(a, w, map, gx, tiles, s);
