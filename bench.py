@@ -18,6 +18,7 @@ CUDA path is checked against) on a bounded row sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import datetime as _dt
 import json
 import os
@@ -36,13 +37,29 @@ METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
 # DRAM bytes per launch of the dominant kernel from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel and the
 # workload; None until a capture of the current kernel exists.
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# `ncu --set full` capture of the bench step (profiles/window_knn1M_bench.md). The
+# counters belong to the kernel build they were taken on: "sources_sha256" is the
+# sha256 of the CUDA sources then (kernel_sources_sha256()), and the bench reports
+# traffic as null once the sources differ.
 NCU_TRAFFIC = {
-    # profiles/window_knn1M_bench.md (ncu --set full, first timed step)
-    "window/knn_1M/N16/sum": 149.0e6,
-    "window/knn_1M/N16/mean": 148.4e6,
-    "window/knn_1M/N64/sum": 558.9e6,
-    "window/knn_1M/N64/mean": 559.0e6,
+    "sources_sha256": "5ae1091692d54419a63e3357371111aeaa50a25ec0b820df00de83bf504e3892",
+    "window/knn_1M/N16/sum": 149.16e6,
+    "window/knn_1M/N16/mean": 148.52e6,
+    "window/knn_1M/N64/sum": 557.58e6,
+    "window/knn_1M/N64/mean": 560.45e6,
 }
+
+
+def kernel_sources_sha256():
+    csrc = os.path.join(ROOT, "sparse_dense_matrix_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(name.encode())
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
 
 FALLBACK_HBM_GBS = 6800.0
 
@@ -350,7 +367,9 @@ def run_ours(args):
     achieved = bytes_dom / (mean_ms[kdom] / 1e3) / 1e9
     key = f"{info['family_name']}/{spec['name']}/N{n_dom}/{r_dom}"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": NCU_TRAFFIC.get(key),
+                "frac": achieved / hbm_peak,
+                "traffic": (NCU_TRAFFIC.get(key) if kernel_sources_sha256() ==
+                            NCU_TRAFFIC["sources_sha256"] else None),
                 "kernel": key, "peak_source": peak_kind,
                 "algorithmic_bytes_per_launch": bytes_dom,
                 "launches_per_run": info["launches"]}
