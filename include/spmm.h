@@ -268,9 +268,14 @@ spmm_status spmm_transpose(spmm_plan_t plan, const int32_t *col, const float *va
  *   dB     : device, fp32 [K, N], written once per element:
  *            dB[j, c] = sum over the entries (i, j) of A with argmax[i, c] == j
  *            of a_ij * dC[i, c] (every stored copy of a duplicated pair counts),
- *            accumulated in fp32 in increasing i; 0 where no row chose j.
- * Asynchronous; no allocation. 128-bit loads when N % 4 == 0 and argmax, dC
- * and dB are 16-byte aligned.
+ *            accumulated in fp32 in increasing i; 0 where no row chose j. Rows
+ *            of A^T longer than planT's split threshold (hub columns of A) are
+ *            cut into planT's chunks: each chunk is summed in increasing i,
+ *            then the chunks in order (no atomics; reproducible).
+ * Asynchronous, except that the first call with split rows at a given N
+ * grows planT's workspace with cudaMalloc (spmm_plan_reserve(planT, N,
+ * SPMM_SUM) beforehand keeps allocation out). 128-bit loads when N % 4 == 0
+ * and argmax, dC and dB are 16-byte aligned.
  */
 spmm_status spmm_maxpool_backward(spmm_plan_t planT, const int32_t *colT, const float *valT,
                                   const int32_t *argmax, const float *dC, int64_t N, float *dB,

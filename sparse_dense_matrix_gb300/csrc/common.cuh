@@ -233,5 +233,7 @@ cudaError_t launch_window(const RunArgs &a, const WinShape &w, int reduce, bool 
                           int grid_x, int tiles, cudaStream_t s);
 bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool has_val,
                   int lanes, int chunks, int rows_per_group, WinShape *out);
+// grow a plan's workspace to at least `need` bytes (cudaMalloc; synchronous)
+spmm_status plan_ensure_workspace(Plan *p, size_t need);
 
 }  // namespace spmm

@@ -330,6 +330,8 @@ spmm_status ensure_workspace(Plan *p, size_t need) {
 
 }  // namespace
 
+spmm_status plan_ensure_workspace(Plan *p, size_t need) { return ensure_workspace(p, need); }
+
 // ------------------------------------------------------------------ router
 // Rules, first match wins (RA-SpMM "routing rules": descriptors + N -> family):
 //   R0  a family pinned by spmm_plan_set_family is used as given (WINDOW only

@@ -183,41 +183,104 @@ __global__ void k_bounds(const uint32_t *keys, int64_t nnz, int64_t K, int32_t *
 // Row j of A^T lists the entries (i, a_ij) of column j of A in increasing i.
 // dB[j, c] = sum over them of a_ij * dC[i, c] where argmax[i, c] == j,
 // accumulated in fp32 in that order. L lanes own a row, V columns per lane
-// per step; a warp holds 32 / L rows.
+// per step; a warp holds 32 / L rows. Rows of A^T longer than t_split (hub
+// columns of A) are left to the split below, as in the forward product.
+template <int V, bool HAS_VAL>
+__device__ __forceinline__ void mp_accumulate(const int32_t *__restrict__ colT,
+                                              const float *__restrict__ valT,
+                                              const int32_t *__restrict__ argmax,
+                                              const float *__restrict__ dC, int64_t N, int j,
+                                              int p0, int p1, int64_t c, float (&acc)[V]) {
+    for (int p = p0; p < p1; ++p) {
+        const int64_t i = colT[p];
+        const float a = HAS_VAL ? valT[p] : 1.0f;
+        float g[V];
+        int w[V];
+        if constexpr (V == 4) {
+            const float4 gv = __ldg(reinterpret_cast<const float4 *>(dC + i * N + c));
+            const int4 wv = __ldg(reinterpret_cast<const int4 *>(argmax + i * N + c));
+            g[0] = gv.x; g[1] = gv.y; g[2] = gv.z; g[3] = gv.w;
+            w[0] = wv.x; w[1] = wv.y; w[2] = wv.z; w[3] = wv.w;
+        } else {
+            g[0] = __ldg(dC + i * N + c);
+            w[0] = __ldg(argmax + i * N + c);
+        }
+#pragma unroll
+        for (int e = 0; e < V; ++e)
+            if (w[e] == j) acc[e] = HAS_VAL ? __fmaf_rn(a, g[e], acc[e]) : __fadd_rn(acc[e], g[e]);
+    }
+}
+
 template <int V, bool HAS_VAL>
 __global__ void __launch_bounds__(256) k_maxpool_bwd(const int32_t *__restrict__ rowptrT,
                                                     const int32_t *__restrict__ colT,
                                                     const float *__restrict__ valT,
                                                     const int32_t *__restrict__ argmax,
                                                     const float *__restrict__ dC, int64_t rows,
-                                                    int64_t N, int lanes, float *__restrict__ dB) {
+                                                    int64_t N, int lanes, int t_split,
+                                                    float *__restrict__ dB) {
     const int lane = threadIdx.x & 31;
     const int sub = lane % lanes, grp = lane / lanes, groups = 32 / lanes;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t j = warp * groups + grp;
     if (j >= rows) return;
     const int p0 = rowptrT[j], p1 = rowptrT[j + 1];
+    if (p1 - p0 > t_split) return;                 // a split row
     for (int64_t c = (int64_t)sub * V; c < N; c += (int64_t)lanes * V) {
         float acc[V];
 #pragma unroll
         for (int e = 0; e < V; ++e) acc[e] = 0.0f;
-        for (int p = p0; p < p1; ++p) {
-            const int64_t i = colT[p];
-            const float a = HAS_VAL ? valT[p] : 1.0f;
-            float g[V];
-            int w[V];
-            if constexpr (V == 4) {
-                const float4 gv = __ldg(reinterpret_cast<const float4 *>(dC + i * N + c));
-                const int4 wv = __ldg(reinterpret_cast<const int4 *>(argmax + i * N + c));
-                g[0] = gv.x; g[1] = gv.y; g[2] = gv.z; g[3] = gv.w;
-                w[0] = wv.x; w[1] = wv.y; w[2] = wv.z; w[3] = wv.w;
-            } else {
-                g[0] = __ldg(dC + i * N + c);
-                w[0] = __ldg(argmax + i * N + c);
-            }
+        mp_accumulate<V, HAS_VAL>(colT, valT, argmax, dC, N, (int)j, p0, p1, c, acc);
+        st_vec<V>(dB + j * N + c, acc);
+    }
+}
+
+// Split rows, phase 1: a warp per chunk of `chunk` entries writes its partial
+// (chunk-local masked sum) to ws[q][:].
+template <int V, bool HAS_VAL>
+__global__ void __launch_bounds__(256) k_maxpool_chunks(const int32_t *__restrict__ rowptrT,
+                                                       const int32_t *__restrict__ colT,
+                                                       const float *__restrict__ valT,
+                                                       const int32_t *__restrict__ argmax,
+                                                       const float *__restrict__ dC, int64_t N,
+                                                       const int2 *__restrict__ chunks,
+                                                       int64_t n_chunks, int chunk,
+                                                       float *__restrict__ ws) {
+    const int lane = threadIdx.x & 31;
+    const int64_t q = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (q >= n_chunks) return;
+    const int2 ch = chunks[q];                      // (row of A^T, first entry)
+    const int p1 = min(ch.y + chunk, rowptrT[ch.x + 1]);
+    for (int64_t c = (int64_t)lane * V; c < N; c += 32 * V) {
+        float acc[V];
 #pragma unroll
-            for (int e = 0; e < V; ++e)
-                if (w[e] == (int)j) acc[e] = HAS_VAL ? __fmaf_rn(a, g[e], acc[e]) : __fadd_rn(acc[e], g[e]);
+        for (int e = 0; e < V; ++e) acc[e] = 0.0f;
+        mp_accumulate<V, HAS_VAL>(colT, valT, argmax, dC, N, ch.x, ch.y, p1, c, acc);
+        st_vec<V>(ws + q * N + c, acc);
+    }
+}
+
+// Split rows, phase 2: a warp per split row adds its chunks' partials in
+// chunk order and writes the row of dB.
+template <int V>
+__global__ void __launch_bounds__(256) k_maxpool_combine(const int32_t *__restrict__ heavy_rows,
+                                                        const int32_t *__restrict__ heavy_chunk0,
+                                                        int64_t n_heavy, int64_t N,
+                                                        const float *__restrict__ ws,
+                                                        float *__restrict__ dB) {
+    const int lane = threadIdx.x & 31;
+    const int64_t h = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (h >= n_heavy) return;
+    const int64_t j = heavy_rows[h];
+    const int q0 = heavy_chunk0[h], q1 = heavy_chunk0[h + 1];
+    for (int64_t c = (int64_t)lane * V; c < N; c += 32 * V) {
+        float acc[V];
+        ld_vec<V>(ws + (int64_t)q0 * N + c, acc);
+        for (int q = q0 + 1; q < q1; ++q) {
+            float x[V];
+            ld_vec<V>(ws + (int64_t)q * N + c, x);
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
         }
         st_vec<V>(dB + j * N + c, acc);
     }
@@ -350,15 +413,38 @@ spmm_status spmm_maxpool_backward(spmm_plan_t planT, const int32_t *colT, const 
     const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
     cudaStream_t s = (cudaStream_t)stream;
     const bool hv = valT != nullptr;
+    Plan *pm = const_cast<Plan *>(p);
+    if (p->n_heavy > 0) {
+        const spmm_status st = plan_ensure_workspace(pm, (size_t)p->n_chunks * (size_t)N * 4);
+        if (st != SPMM_OK) return st;
+    }
+    const int ts = (int)std::min<int64_t>(p->t_split, INT32_MAX);
     if (v4) {
-        if (hv) k_maxpool_bwd<4, true><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, dB);
-        else k_maxpool_bwd<4, false><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, dB);
+        if (hv) k_maxpool_bwd<4, true><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, ts, dB);
+        else k_maxpool_bwd<4, false><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, ts, dB);
     } else {
-        if (hv) k_maxpool_bwd<1, true><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, dB);
-        else k_maxpool_bwd<1, false><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, dB);
+        if (hv) k_maxpool_bwd<1, true><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, ts, dB);
+        else k_maxpool_bwd<1, false><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, ts, dB);
     }
     count_launch();
-    return t_status(cudaGetLastError());
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && p->n_heavy > 0) {
+        float *ws = reinterpret_cast<float *>(pm->work);
+        const unsigned cb = (unsigned)((p->n_chunks + 7) / 8), hb = (unsigned)((p->n_heavy + 7) / 8);
+        const int ch = (int)p->chunk;
+        if (v4) {
+            if (hv) k_maxpool_chunks<4, true><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
+            else k_maxpool_chunks<4, false><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
+            k_maxpool_combine<4><<<hb, 256, 0, s>>>(p->heavy_rows, p->heavy_chunk0, p->n_heavy, N, ws, dB);
+        } else {
+            if (hv) k_maxpool_chunks<1, true><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
+            else k_maxpool_chunks<1, false><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
+            k_maxpool_combine<1><<<hb, 256, 0, s>>>(p->heavy_rows, p->heavy_chunk0, p->n_heavy, N, ws, dB);
+        }
+        count_launch(2);
+        e = cudaGetLastError();
+    }
+    return t_status(e);
 }
 
 }  // extern "C"

@@ -50,7 +50,25 @@ GRAPHS = {
     "k257": lambda: gen.erdos_renyi(9000, 257, 5, seed=6),       # two passes
     "k70000": lambda: gen.erdos_renyi(3000, 70000, 9, seed=7),   # three passes
     "empty": lambda: gen.from_rows("empty", 50, 40, [[] for _ in range(50)]),
+    "hub": lambda: hub_graph(),
 }
+
+
+def hub_graph(M=6000, K=900):
+    """Every row holds column 7 (a row of 6000 entries in A^T, split into
+    chunks) plus a few random columns; some rows repeat column 7."""
+    rng = np.random.default_rng(9)
+    rows, vals = [], []
+    for i in range(M):
+        c = [7] + rng.integers(0, K, size=int(rng.integers(0, 6))).tolist()
+        if i % 11 == 0:
+            c.append(7)
+        rng.shuffle(c)
+        rows.append(c)
+        vals.append(rng.standard_normal(len(c)).astype(np.float32).tolist())
+    return gen.from_rows("hub", M, K, rows, vals)
+
+
 _cache = {}
 
 
@@ -138,10 +156,21 @@ def check_maxpool(sdm, dev, g, N, seed=0):
 
 
 @pytest.mark.parametrize("name", ["er", "knn_weighted", "rmat", "chung_lu", "dup",
-                                  "dup_unweighted", "k1", "empty"])
+                                  "dup_unweighted", "k1", "empty", "hub"])
 @pytest.mark.parametrize("N", [1, 16, 33, 64, 130])
 def test_maxpool_backward(sdm, cuda_device, name, N):
     check_maxpool(sdm, cuda_device, graph(name), N)
+
+
+def test_maxpool_backward_split_rows(sdm, cuda_device):
+    """The hub column's row of A^T exceeds the split threshold."""
+    g = graph("hub")
+    adj = make_adj(sdm, g, cuda_device)
+    t = adj.transpose()
+    assert t.describe(16)["n_heavy"] >= 1
+    t.close()
+    adj.close()
+    check_maxpool(sdm, cuda_device, g, 16)
 
 
 def test_maxpool_backward_deterministic(sdm, cuda_device):
