@@ -49,6 +49,9 @@ typedef enum {
 /* graph-spmm model card, "API": spmm_sum / spmm_mean / spmm_max. */
 typedef enum { SPMM_SUM = 0, SPMM_MEAN = 1, SPMM_MAX = 2 } spmm_reduce;
 
+/* Activation of the fused epilogue (spmm_run_ex). */
+typedef enum { SPMM_ACT_NONE = 0, SPMM_ACT_RELU = 1 } spmm_activation;
+
 /* Kernel families the router chooses among (RA-SpMM "kernel portfolio" and
  * "routing rules": the family is picked from the descriptors and N). */
 typedef enum {
@@ -140,6 +143,23 @@ spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *
  */
 spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, const float *B,
                      int64_t N, spmm_reduce reduce, float *C, int32_t *argmax, void *stream);
+
+/*
+ * spmm_run_ex -- spmm_run with a fused epilogue on every output element
+ * (GraphSPMM, "SpMM fused with the layer's epilogue": the bias and the
+ * activation are applied where C is written, so C makes one trip to memory):
+ *   C[i,k] = act(R[i,k] + bias[k])
+ * with R the reduction's value as spmm_run defines it (empty rows included:
+ * R = 0), the addition in fp32 (round to nearest) and act applied after it.
+ *   bias : device, fp32 [N], or NULL for no bias.
+ *   act  : SPMM_ACT_NONE, or SPMM_ACT_RELU (x > 0 ? x : +0).
+ * argmax (SPMM_MAX) is the reduction's and is not affected. Everything else,
+ * including the error behaviour, is as in spmm_run; an unknown act returns
+ * SPMM_ERR_INVALID_ARG. spmm_run(...) is spmm_run_ex(..., NULL, SPMM_ACT_NONE, ...).
+ */
+spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, const float *B,
+                        int64_t N, spmm_reduce reduce, const float *bias, spmm_activation act,
+                        float *C, int32_t *argmax, void *stream);
 
 /*
  * spmm_plan_reserve -- allocate the workspace spmm_run needs for (N, reduce)

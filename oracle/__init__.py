@@ -38,6 +38,7 @@ _lock = threading.Lock()
 _lib = None
 
 REDUCE = {"sum": 0, "mean": 1, "max": 2}
+ACT = {"none": 0, "relu": 1}
 
 
 class _Desc(ctypes.Structure):
@@ -75,6 +76,9 @@ class Oracle:
         i64 = ctypes.c_int64
         lib.oracle_spmm_rows.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int, p, i64, p, p, p]
         lib.oracle_spmm_rows.restype = ctypes.c_int
+        lib.oracle_spmm_rows_ex.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int, p, ctypes.c_int,
+                                            p, i64, p, p, p]
+        lib.oracle_spmm_rows_ex.restype = ctypes.c_int
         lib.oracle_descriptors.argtypes = [i64, p, ctypes.POINTER(_Desc)]
         lib.oracle_descriptors.restype = ctypes.c_int
         lib.oracle_threads.restype = ctypes.c_int
@@ -87,7 +91,7 @@ class Oracle:
     def threads(self) -> int:
         return int(self.lib.oracle_threads())
 
-    def spmm(self, rowptr, col, val, B, reduce: str, rows=None, K=None):
+    def spmm(self, rowptr, col, val, B, reduce: str, rows=None, K=None, bias=None, act="none"):
         rowptr = np.ascontiguousarray(rowptr, dtype=np.int32)
         col = np.ascontiguousarray(col, dtype=np.int32)
         val = None if val is None else np.ascontiguousarray(val, dtype=np.float32)
@@ -106,8 +110,13 @@ class Oracle:
         C = np.empty((R, N), dtype=np.float32)
         A = np.empty((R, N), dtype=np.int32) if red == 2 else None
         T = np.empty((R, N), dtype=np.float32) if red != 2 else None
-        rc = self.lib.oracle_spmm_rows(M, K, N, _ptr(rowptr), _ptr(col), _ptr(val), _ptr(B), red,
-                                       _ptr(rows_arr), R, _ptr(C), _ptr(A), _ptr(T))
+        if bias is not None:
+            bias = np.ascontiguousarray(bias, dtype=np.float32)
+            if bias.shape != (N,):
+                raise ValueError("bias must hold N values")
+        rc = self.lib.oracle_spmm_rows_ex(M, K, N, _ptr(rowptr), _ptr(col), _ptr(val), _ptr(B), red,
+                                          _ptr(bias), ACT[act], _ptr(rows_arr), R, _ptr(C),
+                                          _ptr(A), _ptr(T))
         if rc != 0:
             raise ValueError("oracle_spmm_rows rejected its arguments")
         return C, A, T
@@ -168,12 +177,14 @@ def threads() -> int:
     return _default().threads()
 
 
-def spmm(rowptr, col, val, B, reduce: str, rows=None, K=None):
+def spmm(rowptr, col, val, B, reduce: str, rows=None, K=None, bias=None, act="none"):
     """Oracle SpMM. Returns (C float32 [R,N], argmax int32 [R,N] or None, T float32 [R,N] or None).
 
-    ``rows`` selects output rows (int64 array); None means all M rows.
+    ``rows`` selects output rows (int64 array); None means all M rows. ``bias``
+    (float32 [N]) and ``act`` ("none" or "relu") give the fused epilogue
+    act(R + bias); T is the tolerance scale of the reduction alone.
     """
-    return _default().spmm(rowptr, col, val, B, reduce, rows, K)
+    return _default().spmm(rowptr, col, val, B, reduce, rows, K, bias, act)
 
 
 def descriptors(rowptr) -> dict:

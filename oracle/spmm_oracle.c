@@ -33,6 +33,13 @@
  *   T[i,k] = sum_p |x_p| is returned beside sum/mean as the scale of the
  *   floating-point tolerance |err| <= 1e-5 * T + 1e-6.
  *
+ * Epilogue (GraphSPMM: the SpMM fused with the layer's bias and activation):
+ *   with a bias vector b [N] and/or ReLU, the output is
+ *   act(R[i,k] + b[k]) where R is the value defined above before its final
+ *   rounding (the fp64 sum, or the fp64 mean, or the fp32 max), the addition
+ *   is done in fp64 and rounded to fp32 once, and ReLU(x) = x > 0 ? x : +0 is
+ *   applied last. An empty row has R = 0. argmax is not affected.
+ *
  * Descriptors (RA-SpMM abstract and "routing rules": one O(M) pass over the
  * row pointers gives M, the mean row degree and the coefficient of variation
  * of the row degree): dbar = nnz / M and CV_d = std(d) / mean(d), std taken
@@ -51,6 +58,7 @@
 #endif
 
 enum { ORACLE_SUM = 0, ORACLE_MEAN = 1, ORACLE_MAX = 2 };
+enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_RELU = 1 };
 
 /* Mutation switch for the pin tests only: a build with -DORACLE_PLANT=n plants
  * one known mistake so the tests can show that their pins reject it.
@@ -72,16 +80,28 @@ int oracle_threads(void) {
 #endif
 }
 
+/* The epilogue on one value r (fp64): add the bias, round once, then ReLU. */
+static float oracle_epilogue(double r, const float *bias, int64_t k, int act) {
+#if ORACLE_PLANT == 6
+    if (act == ORACLE_ACT_RELU) r = r > 0.0 ? r : 0.0;   /* planted: ReLU before the bias */
+    return (float)(bias ? r + (double)bias[k] : r);
+#else
+    float c = (float)(bias ? r + (double)bias[k] : r);
+    if (act == ORACLE_ACT_RELU) c = c > 0.0f ? c : 0.0f;
+    return c;
+#endif
+}
+
 /* One output row. S and Tacc are caller scratch of N doubles each. */
 static void oracle_row(int64_t i, int64_t K, int64_t N, const int32_t *rowptr, const int32_t *col,
-                       const float *val, const float *B, int reduce, float *Crow,
-                       int32_t *Arow, float *Trow, double *S, double *Tacc) {
+                       const float *val, const float *B, int reduce, const float *bias, int act,
+                       float *Crow, int32_t *Arow, float *Trow, double *S, double *Tacc) {
     const int64_t p0 = rowptr[i], p1 = rowptr[i + 1];
     const int64_t d = p1 - p0;
     if (reduce == ORACLE_MAX) {
         if (d == 0) {
             for (int64_t k = 0; k < N; ++k) {
-                Crow[k] = 0.0f;
+                Crow[k] = oracle_epilogue(0.0, bias, k, act);
                 if (Arow) Arow[k] = -1;
             }
             return;
@@ -119,6 +139,8 @@ static void oracle_row(int64_t i, int64_t K, int64_t N, const int32_t *rowptr, c
             }
         }
         free(tmp);
+        if (bias || act != ORACLE_ACT_NONE)
+            for (int64_t k = 0; k < N; ++k) Crow[k] = oracle_epilogue((double)Crow[k], bias, k, act);
         return;
     }
     for (int64_t k = 0; k < N; ++k) {
@@ -146,14 +168,16 @@ static void oracle_row(int64_t i, int64_t K, int64_t N, const int32_t *rowptr, c
         }
     }
     for (int64_t k = 0; k < N; ++k) {
+        double r;
         if (reduce == ORACLE_MEAN)
 #if ORACLE_PLANT == 5
-            Crow[k] = d ? (float)(S[k] / (double)(d + 1)) : 0.0f;  /* planted: wrong divisor */
+            r = d ? S[k] / (double)(d + 1) : 0.0;  /* planted: wrong divisor */
 #else
-            Crow[k] = d ? (float)(S[k] / (double)d) : 0.0f;
+            r = d ? S[k] / (double)d : 0.0;
 #endif
         else
-            Crow[k] = (float)S[k];
+            r = S[k];
+        Crow[k] = oracle_epilogue(r, bias, k, act);
         if (Trow) Trow[k] = (float)Tacc[k];
     }
 }
@@ -161,11 +185,13 @@ static void oracle_row(int64_t i, int64_t K, int64_t N, const int32_t *rowptr, c
 /* Rows given by `rows` (nrows of them; NULL means rows 0..M-1 in order).
  * Output row r of C / argmax / T corresponds to input row rows[r].
  * Returns 0, or -1 on a bad argument (the caller sees it as an exception). */
-int oracle_spmm_rows(int64_t M, int64_t K, int64_t N, const int32_t *rowptr,
-                     const int32_t *col, const float *val, const float *B, int reduce,
-                     const int64_t *rows, int64_t nrows, float *C, int32_t *argmax, float *T) {
+int oracle_spmm_rows_ex(int64_t M, int64_t K, int64_t N, const int32_t *rowptr,
+                        const int32_t *col, const float *val, const float *B, int reduce,
+                        const float *bias, int act, const int64_t *rows, int64_t nrows, float *C,
+                        int32_t *argmax, float *T) {
     if (M < 0 || K < 0 || N < 0 || nrows < 0 || !rowptr || !C) return -1;
     if (reduce < ORACLE_SUM || reduce > ORACLE_MAX) return -1;
+    if (act != ORACLE_ACT_NONE && act != ORACLE_ACT_RELU) return -1;
     if (rows) {
         for (int64_t r = 0; r < nrows; ++r)
             if (rows[r] < 0 || rows[r] >= M) return -1;
@@ -180,13 +206,20 @@ int oracle_spmm_rows(int64_t M, int64_t K, int64_t N, const int32_t *rowptr,
         for (int64_t r = 0; r < nrows; ++r) {
             if (!S || !Tacc) continue;
             const int64_t i = rows ? rows[r] : r;
-            oracle_row(i, K, N, rowptr, col, val, B, reduce, C + r * N,
+            oracle_row(i, K, N, rowptr, col, val, B, reduce, bias, act, C + r * N,
                        argmax ? argmax + r * N : NULL, T ? T + r * N : NULL, S, Tacc);
         }
         free(S);
         free(Tacc);
     }
     return bad ? -1 : 0;
+}
+
+int oracle_spmm_rows(int64_t M, int64_t K, int64_t N, const int32_t *rowptr,
+                     const int32_t *col, const float *val, const float *B, int reduce,
+                     const int64_t *rows, int64_t nrows, float *C, int32_t *argmax, float *T) {
+    return oracle_spmm_rows_ex(M, K, N, rowptr, col, val, B, reduce, NULL, ORACLE_ACT_NONE, rows,
+                               nrows, C, argmax, T);
 }
 
 int oracle_spmm(int64_t M, int64_t K, int64_t N, const int32_t *rowptr, const int32_t *col,

@@ -30,11 +30,12 @@ __all__ = [
     "spmm_plan_create", "spmm_run", "spmm_plan_describe", "spmm_plan_destroy",
     "spmm_plan_reserve", "spmm_plan_validate_cols", "spmm_plan_sync", "spmm_plan_set_family",
     "spmm_route", "spmm_default_t_split", "spmm_status_string", "spmm_launch_count",
-    "spmm_run_noalloc", "spmm_transpose", "spmm_maxpool_backward",
+    "spmm_run_noalloc", "spmm_transpose", "spmm_maxpool_backward", "spmm_run_ex", "ACT",
     "PlanInfo", "REDUCE", "FAMILY", "lib", "build_library",
 ]
 
 REDUCE = {"sum": 0, "mean": 1, "max": 2}
+ACT = {None: 0, "none": 0, "relu": 1}
 FAMILY = {"auto": -1, "rowgroup": 0, "warprow": 1, "coltile": 2, "window": 3}
 STATUS = {0: "SPMM_OK", 1: "SPMM_ERR_INVALID_ARG", 2: "SPMM_ERR_INVALID_INPUT", 3: "SPMM_ERR_OOM",
           4: "SPMM_ERR_CUDA", 5: "SPMM_ERR_UNSUPPORTED", 6: "SPMM_ERR_TIMEOUT"}
@@ -80,6 +81,7 @@ def _load():
     sigs = {
         "spmm_plan_create": ([vp, i64, i64, vp, P(vp)], i32),
         "spmm_run": ([vp, vp, vp, vp, i64, i32, vp, vp, vp], i32),
+        "spmm_run_ex": ([vp, vp, vp, vp, i64, i32, vp, i32, vp, vp, vp], i32),
         "spmm_plan_reserve": ([vp, i64, i32], i32),
         "spmm_plan_validate_cols": ([vp, vp, vp], i32),
         "spmm_plan_sync": ([vp, vp], i32),
@@ -140,6 +142,13 @@ def spmm_run(plan: int, col_ptr: int, val_ptr, B_ptr: int, N: int, reduce: int, 
              argmax_ptr=None, stream=None) -> None:
     _check(lib.spmm_run(plan, col_ptr, val_ptr, B_ptr, N, reduce, C_ptr, argmax_ptr,
                         _stream_handle(stream)), "spmm_run")
+
+
+def spmm_run_ex(plan: int, col_ptr: int, val_ptr, B_ptr: int, N: int, reduce: int, bias_ptr,
+                act: int, C_ptr: int, argmax_ptr=None, stream=None) -> None:
+    """spmm_run with the fused epilogue C = act(R + bias)."""
+    _check(lib.spmm_run_ex(plan, col_ptr, val_ptr, B_ptr, N, reduce, bias_ptr, act, C_ptr,
+                           argmax_ptr, _stream_handle(stream)), "spmm_run_ex")
 
 
 def spmm_plan_reserve(plan: int, N: int, reduce: int) -> None:
@@ -277,11 +286,17 @@ class SparseAdj:
         with torch.cuda.device(self.device):
             spmm_plan_reserve(self.plan, N, REDUCE[reduce])
 
-    def reduce(self, mat, reduce: str = "sum", out=None, argmax=None, stream=None):
-        """sum / mean -> C [M, N]; max -> (C, argmax int32 [M, N])."""
+    def reduce(self, mat, reduce: str = "sum", out=None, argmax=None, stream=None, bias=None,
+               activation=None):
+        """sum / mean -> C [M, N]; max -> (C, argmax int32 [M, N]).
+
+        ``bias`` (float32 [N]) and ``activation`` (None or "relu") fuse the
+        epilogue C = act(R + bias) into the same launch."""
         import torch
         if reduce not in REDUCE:
             raise ValueError(f"unknown reduce {reduce!r}")
+        if activation not in ACT:
+            raise ValueError(f"unknown activation {activation!r}")
         _req(mat, torch.float32, "mat", self.device)
         if mat.dim() != 2 or mat.shape[0] != self.K:
             raise ValueError(f"mat must be [{self.K}, N], got {tuple(mat.shape)}")
@@ -300,11 +315,16 @@ class SparseAdj:
                 _req(argmax, torch.int32, "argmax", self.device)
                 if tuple(argmax.shape) != (self.M, N):
                     raise ValueError("argmax has the wrong shape")
+        if bias is not None:
+            _req(bias, torch.float32, "bias", self.device)
+            if tuple(bias.shape) != (N,):
+                raise ValueError(f"bias must be [{N}]")
         with torch.cuda.device(self.device):
-            spmm_run(self.plan, self.col.data_ptr(),
-                     None if self.val is None else self.val.data_ptr(),
-                     mat.data_ptr(), N, red, out.data_ptr(),
-                     argmax.data_ptr() if red == 2 else None, stream)
+            spmm_run_ex(self.plan, self.col.data_ptr(),
+                        None if self.val is None else self.val.data_ptr(),
+                        mat.data_ptr(), N, red, None if bias is None else bias.data_ptr(),
+                        ACT[activation], out.data_ptr(), argmax.data_ptr() if red == 2 else None,
+                        stream)
         return (out, argmax) if red == 2 else out
 
     def __matmul__(self, mat):

@@ -94,7 +94,24 @@ struct RunArgs {
     float *__restrict__ ws_val;               // [n_chunks][N]
     int32_t *__restrict__ ws_arg;             // [n_chunks][N] (max only)
     int32_t *__restrict__ err;
+    const float *__restrict__ bias;           // [N] added to every output row, or NULL
+    int32_t act;                              // spmm_activation applied after the bias
 };
+
+// Fused epilogue on V consecutive outputs starting at column c: C = act(C + bias)
+// (GraphSPMM-style "SpMM followed by an epilogue"; the argmax of max is not
+// affected). ReLU is x > 0 ? x : +0, so -0 and negative values give +0.
+template <int V>
+__device__ __forceinline__ void epilogue(const RunArgs &a, int64_t c, float (&out)[V]) {
+    if (a.bias) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) out[e] = __fadd_rn(out[e], __ldg(a.bias + c + e));
+    }
+    if (a.act == SPMM_ACT_RELU) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) out[e] = out[e] > 0.0f ? out[e] : 0.0f;
+    }
+}
 
 // --- global loads / stores with cache hints --------------------------------
 // Gathered B rows are re-read by other rows: keep them in L1/L2 (ld.global.nc).

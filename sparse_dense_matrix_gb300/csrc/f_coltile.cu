@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(kCtThreads) k_coltile(const RunArgs a, int wpr
     float out[4];
     int arg[4];
     acc.finish(s_d[rs], out, arg);
+    epilogue<4>(a, c, out);
     const int64_t i = r0 + rs;
     st_vec<4>(a.C + i * N + c, out);
     if (RED == SPMM_MAX && a.argmax) st_vec_i<4>(a.argmax + i * N + c, arg);

@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(256) k_rowgroup(const RunArgs a) {
     float out[V];
     int arg[V];
     acc.finish(d, out, arg);
+    epilogue<V>(a, (int64_t)vi * V, out);
     st_vec<V>(a.C + row * N + (int64_t)vi * V, out);
     if (RED == SPMM_MAX && a.argmax) st_vec_i<V>(a.argmax + row * N + (int64_t)vi * V, arg);
 }

@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(256) k_warprow(const RunArgs a) {
     int arg[V];
     acc.finish(d, out, arg);
     const int64_t N = a.N;
+    epilogue<V>(a, (int64_t)vi * V, out);
     st_vec<V>(a.C + row * N + (int64_t)vi * V, out);
     if (RED == SPMM_MAX && a.argmax) st_vec_i<V>(a.argmax + row * N + (int64_t)vi * V, arg);
 }
@@ -153,6 +154,7 @@ __global__ void __launch_bounds__(128) k_heavy_combine(const RunArgs a) {
 #pragma unroll
             for (int e = 0; e < V; ++e) acc[e] = __fmul_rn(acc[e], inv_d);
         }
+        epilogue<V>(a, col0, acc);
         st_vec<V>(a.C + (int64_t)row * N + col0, acc);
         if constexpr (RED == SPMM_MAX) {
             if (a.argmax) st_vec_i<V>(a.argmax + (int64_t)row * N + col0, arg);

@@ -637,7 +637,14 @@ spmm_status spmm_plan_sync(spmm_plan_t plan, void *stream) {
 
 spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, const float *B,
                      int64_t N, spmm_reduce reduce, float *C, int32_t *argmax, void *stream) {
+    return spmm_run_ex(plan, col, val, B, N, reduce, nullptr, SPMM_ACT_NONE, C, argmax, stream);
+}
+
+spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, const float *B,
+                        int64_t N, spmm_reduce reduce, const float *bias, spmm_activation act,
+                        float *C, int32_t *argmax, void *stream) {
     if (!plan || N < 0 || reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
+    if (act != SPMM_ACT_NONE && act != SPMM_ACT_RELU) return SPMM_ERR_INVALID_ARG;
     Plan *p = reinterpret_cast<Plan *>(plan);
     if (p->M == 0 || N == 0) return SPMM_OK;
     if (!C) return SPMM_ERR_INVALID_ARG;
@@ -674,6 +681,8 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
     a.heavy_rows = p->heavy_rows;
     a.heavy_chunk0 = p->heavy_chunk0;
     a.err = p->err;
+    a.bias = bias;
+    a.act = (int32_t)act;
     if (p->n_heavy > 0) {
         spmm_status st = ensure_workspace(p, workspace_need(p, N, reduce));
         if (st != SPMM_OK) return st;

@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(kWinThreads, 1)
             float out[4];
             int arg[4];
             acc[k].finish(d, out, arg);
+            epilogue<4>(a, cq[k], out);
             st_vec<4>(a.C + i * N + cq[k], out);
             if (RED == SPMM_MAX && a.argmax) st_vec_i<4>(a.argmax + i * N + cq[k], arg);
         }

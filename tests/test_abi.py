@@ -137,7 +137,7 @@ def test_router_window_rule(sdm):
     knn = dict(_desc(cv=0.0), band_w=512, band_cover=0.999)
     r = sdm.spmm_route(knn, 16, 0)
     assert (r["family_name"], r["lanes"], r["window_chunks"], r["col_tiles"], r["window_rows"]) == \
-        ("window", 2, 2, 1, 256)
+        ("window", 4, 1, 1, 256)
     assert 0 < r["window_smem"] <= 227 * 1024 and r["window_ctas"] == 152
     r = sdm.spmm_route(knn, 64, 1)
     assert (r["family_name"], r["lanes"], r["window_chunks"], r["col_tiles"], r["window_ctas"]) == \

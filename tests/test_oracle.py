@@ -223,6 +223,50 @@ def pin_row_subset_matches_full(o):
             assert np.array_equal(Ts, Tf[rows])
 
 
+def _relu(x):
+    return np.where(x > 0, x, np.float32(0.0)).astype(np.float32)
+
+
+def pin_epilogue_identity_graph(o):
+    # identity: R = B exactly, so act(R + bias) is one fp64 addition rounded once
+    M, N = 40, 9
+    g = gen.from_rows("eye", M, M, [[i] for i in range(M)])
+    B = gen.features(M, N, seed=5)
+    bias = gen.features(1, N, seed=6)[0]
+    want = (B.astype(np.float64) + bias.astype(np.float64)).astype(np.float32)
+    for red in ("sum", "mean", "max"):
+        C, A, _ = o.spmm(g.rowptr, g.col, g.val, B, red, bias=bias)
+        assert np.array_equal(C, want), red
+        C, A, _ = o.spmm(g.rowptr, g.col, g.val, B, red, bias=bias, act="relu")
+        assert np.array_equal(C, _relu(want)), red
+        if red == "max":
+            assert np.array_equal(A, np.repeat(np.arange(M, dtype=np.int32)[:, None], N, 1))
+        C, _, _ = o.spmm(g.rowptr, g.col, g.val, B, red, act="relu")
+        assert np.array_equal(C, _relu(B)), red
+
+
+def pin_epilogue_ring_graph_and_empty_rows(o):
+    # ring: R = B[i-1] + B[i+1] (exact in fp64), mean R / 2 (exact); empty rows R = 0
+    M, N = 31, 6
+    rows = [[(i - 1) % M, (i + 1) % M] if i % 5 else [] for i in range(M)]
+    g = gen.from_rows("ring_holes", M, M, rows)
+    B = gen.features(M, N, seed=7)
+    bias = gen.features(1, N, seed=8)[0].astype(np.float64)
+    B64 = B.astype(np.float64)
+    S = np.zeros((M, N))
+    for i in range(M):
+        if rows[i]:
+            S[i] = B64[(i - 1) % M] + B64[(i + 1) % M]
+    for red, R in (("sum", S), ("mean", S / 2)):
+        want = _relu((R + bias).astype(np.float32))
+        C, _, _ = o.spmm(g.rowptr, g.col, g.val, B, red, bias=bias.astype(np.float32), act="relu")
+        assert np.array_equal(C, want), red
+    C, A, _ = o.spmm(g.rowptr, g.col, g.val, B, "max", bias=bias.astype(np.float32), act="relu")
+    empty = np.array([not r for r in rows])
+    assert np.array_equal(C[empty], np.tile(_relu(bias.astype(np.float32)), (int(empty.sum()), 1)))
+    assert np.all(A[empty] == -1)
+
+
 def pin_descriptors_closed_forms(o):
     d = o.descriptors(np.arange(0, 41, 4, dtype=np.int32))      # 10 rows of degree 4
     assert d["M"] == 10 and d["nnz"] == 40 and d["dbar"] == 4.0 and d["cv"] == 0.0
@@ -259,7 +303,7 @@ def test_oracle_pin(name):
 # planted mistake -> a description; each must be rejected by at least one pin
 PLANTS = {1: "drops the last term of each row", 2: "reads the wrong B row (col + 1)",
           3: "transposed B operand", 4: "max ties go to the larger column",
-          5: "mean divides by d + 1"}
+          5: "mean divides by d + 1", 6: "ReLU applied before the bias"}
 
 
 @pytest.mark.parametrize("n", sorted(PLANTS))
