@@ -60,9 +60,15 @@ typedef enum {
     SPMM_FAMILY_WARPROW = 1,   /* one warp per row, lane groups split the row's entries   */
     SPMM_FAMILY_COLTILE = 2,   /* a CTA per row block, warps own 128-column tiles, col/val
                                   staged in shared memory (wide N)                         */
-    SPMM_FAMILY_WINDOW = 3     /* persistent CTAs over contiguous row ranges; the B rows of a
+    SPMM_FAMILY_WINDOW = 3,    /* persistent CTAs over contiguous row ranges; the B rows of a
                                   sliding window [r0 - W, r1 + W) are streamed into shared
                                   memory by bulk copies (column-locality graphs)           */
+    SPMM_FAMILY_BLOCK = 4      /* block-diagonal graphs: each 128-row tile's 256-column
+                                  diagonal block is densified and multiplied on the tensor
+                                  cores (split TF32, fp32 accumulation); the entries outside
+                                  the block are added by the same CTA. Sum and mean, N % 16
+                                  == 0, aligned B and C. Used only when pinned with
+                                  spmm_plan_set_family (the router does not choose it)     */
 } spmm_family;
 
 typedef struct spmm_plan_s *spmm_plan_t;
@@ -101,6 +107,9 @@ typedef struct {
     int32_t window_ctas;    /* WINDOW family: CTAs per column tile                      */
     int64_t window_smem;    /* WINDOW family: dynamic shared memory per CTA, bytes      */
     int32_t window_chunks;  /* WINDOW family: 4-column chunks per lane (cw = 4 lanes x chunks) */
+    /* block structure, known after spmm_plan_validate_cols (0 before) */
+    int32_t rows_sorted;    /* 1 if every row's columns are non-decreasing             */
+    int64_t blk_intra;      /* entries with col / 256 == row / 256 (diagonal blocks)     */
 } spmm_plan_info;
 
 /*

@@ -36,7 +36,7 @@ __all__ = [
 
 REDUCE = {"sum": 0, "mean": 1, "max": 2}
 ACT = {None: 0, "none": 0, "relu": 1}
-FAMILY = {"auto": -1, "rowgroup": 0, "warprow": 1, "coltile": 2, "window": 3}
+FAMILY = {"auto": -1, "rowgroup": 0, "warprow": 1, "coltile": 2, "window": 3, "block": 4}
 STATUS = {0: "SPMM_OK", 1: "SPMM_ERR_INVALID_ARG", 2: "SPMM_ERR_INVALID_INPUT", 3: "SPMM_ERR_OOM",
           4: "SPMM_ERR_CUDA", 5: "SPMM_ERR_UNSUPPORTED", 6: "SPMM_ERR_TIMEOUT"}
 
@@ -55,6 +55,7 @@ class PlanInfo(ctypes.Structure):
         ("band_w", ctypes.c_int64), ("band_cover", ctypes.c_double),
         ("window_rows", ctypes.c_int32), ("window_ctas", ctypes.c_int32),
         ("window_smem", ctypes.c_int64), ("window_chunks", ctypes.c_int32),
+        ("rows_sorted", ctypes.c_int32), ("blk_intra", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
@@ -187,7 +188,7 @@ def spmm_route(desc: dict, N: int, reduce: int, aligned: int = 3, num_sms: int =
     """
     d = PlanInfo()
     for k in ("M", "K", "nnz", "d_max", "n_empty", "dbar", "cv", "t_split", "chunk",
-              "n_heavy", "n_chunks", "band_w", "band_cover"):
+              "n_heavy", "n_chunks", "band_w", "band_cover", "rows_sorted", "blk_intra"):
         if k in desc:
             setattr(d, k, desc[k])
     out = PlanInfo()

@@ -15,6 +15,7 @@ namespace spmm {
 
 constexpr int kWarp = 32;
 constexpr int kMaxTilesY = 65535;
+constexpr int kBlockRows = 256;     // diagonal block of the BLOCK (tensor-core) family
 
 // Everything a plan owns. Host-side object; the pointers are device memory.
 struct Plan {
@@ -49,6 +50,8 @@ struct Plan {
     int64_t band_w = 0;              // window half-width chosen from the histogram (0: none)
     bool band_all = false;           // every entry has |col - row| <= band_w
     double band_cover = 0.0;         // fraction of entries with |col - row| <= band_w
+    int64_t blk_intra = 0;           // entries inside their row's diagonal kBlockRows block
+    bool rows_sorted = false;        // every row's columns non-decreasing
 };
 
 // Launch shape of the WINDOW family (host-computed; see f_window.cu).
@@ -96,6 +99,7 @@ struct RunArgs {
     int32_t *__restrict__ err;
     const float *__restrict__ bias;           // [N] added to every output row, or NULL
     int32_t act;                              // spmm_activation applied after the bias
+    int32_t rows_sorted;                      // columns non-decreasing within every row
 };
 
 // Fused epilogue on V consecutive outputs starting at column c: C = act(C + bias)
@@ -250,6 +254,7 @@ cudaError_t launch_window(const RunArgs &a, const WinShape &w, int reduce, bool 
                           int grid_x, int tiles, cudaStream_t s);
 bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool has_val,
                   int lanes, int chunks, int rows_per_group, WinShape *out);
+cudaError_t launch_block(const RunArgs &a, int reduce, bool has_val, cudaStream_t s);
 // grow a plan's workspace to at least `need` bytes (cudaMalloc; synchronous)
 spmm_status plan_ensure_workspace(Plan *p, size_t need);
 

@@ -156,12 +156,16 @@ __global__ void __launch_bounds__(kDescThreads) k_heavy_list(const int32_t *__re
 // (b = 0 for distances 0 and 1). Warp-aggregated shared-memory counters, one
 // global add per bin per block (integer counts: the result is exact).
 constexpr int kSpreadBins = 34;
+// two more counters after the spread bins: entries inside their row's diagonal
+// block of kBlockRows x kBlockRows (col / kBlockRows == row / kBlockRows), and
+// entries whose column is below the previous entry's in the same row
+constexpr int kHistWords = kSpreadBins + 2;
 __global__ void __launch_bounds__(256) k_check_cols(const int32_t *__restrict__ rowptr,
                                                    const int32_t *__restrict__ col, int64_t M,
                                                    int64_t K, int32_t *__restrict__ err,
                                                    unsigned long long *__restrict__ hist) {
-    __shared__ unsigned int sh[kSpreadBins];
-    for (int b = threadIdx.x; b < kSpreadBins; b += blockDim.x) sh[b] = 0;
+    __shared__ unsigned int sh[kHistWords];
+    for (int b = threadIdx.x; b < kHistWords; b += blockDim.x) sh[b] = 0;
     __syncthreads();
     int bad = 0;
     const int lane = threadIdx.x & 31;
@@ -172,22 +176,29 @@ __global__ void __launch_bounds__(256) k_check_cols(const int32_t *__restrict__ 
         for (int pb = p0; pb < p1; pb += 32) {
             const int p = pb + lane;
             int b = -1;
+            bool in_blk = false, descent = false;
             if (p < p1) {
                 const int c = col[p];
+                descent = p > p0 && c < col[p - 1];
                 if (c < 0 || (int64_t)c >= K) {
                     bad = 1;
                 } else {
                     const unsigned long long dist =
                         (unsigned long long)((int64_t)c > row ? (int64_t)c - row : row - (int64_t)c);
                     b = dist <= 1 ? 0 : 64 - __clzll((long long)(dist - 1));
+                    in_blk = ((int64_t)c / kBlockRows) == (row / kBlockRows);
                 }
             }
             const unsigned peers = __match_any_sync(__activemask(), b);
             if (b >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sh[b], (unsigned)__popc(peers));
+            const unsigned nb = __popc(__ballot_sync(__activemask(), in_blk));
+            if (lane == 0 && nb) atomicAdd(&sh[kSpreadBins], nb);
+            const unsigned nd = __popc(__ballot_sync(__activemask(), descent));
+            if (lane == 0 && nd) atomicAdd(&sh[kSpreadBins + 1], nd);
         }
     }
     __syncthreads();
-    for (int b = threadIdx.x; b < kSpreadBins; b += blockDim.x)
+    for (int b = threadIdx.x; b < kHistWords; b += blockDim.x)
         if (sh[b]) atomicAdd(&hist[b], (unsigned long long)sh[b]);
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err + kErrBadCol, 1);
 }
@@ -371,8 +382,16 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     const bool window_ok = (family_override == SPMM_FAMILY_AUTO || forced) &&
                            d->band_w > 0 && (aligned & 3) == 3 && N > 0 && N % 4 == 0 &&
                            (forced || (d->dbar >= 2.0 && d->band_cover >= 0.97)) && d->M > 0;
+    // R1a: BLOCK (tensor cores) only when pinned. It is correct on any graph,
+    // but on the 64k-row community graph (51 of 56 entries per row inside the
+    // 256-column diagonal blocks, block density 0.2) it measured 145 us at
+    // N=128 against 94 us for WARPROW: the per-chunk staging of the operands,
+    // not the tensor cores, bounds it. The router keeps it out until it wins.
+    if (family_override == SPMM_FAMILY_BLOCK && d->M > 0 && N > 0 && N % 16 == 0 &&
+        (aligned & 1) && reduce != SPMM_MAX)
+        fam = SPMM_FAMILY_BLOCK;
     int64_t win_tiles = 0;
-    if (window_ok) {
+    if (window_ok && fam == -2) {
         bool found = false;
         // column tiles of cw = 4 L Q columns, widest first: Q = 2 chunks per lane
         // (L = cw / 8) down to cw = 16, then L = 2, Q = 1 for cw = 8
@@ -412,7 +431,8 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     if (fam == -2) {
         if (family_override == SPMM_FAMILY_COLTILE)
             fam = coltile_ok ? SPMM_FAMILY_COLTILE : SPMM_FAMILY_WARPROW;
-        else if (family_override != SPMM_FAMILY_AUTO && family_override != SPMM_FAMILY_WINDOW)
+        else if (family_override != SPMM_FAMILY_AUTO && family_override != SPMM_FAMILY_WINDOW &&
+                 family_override != SPMM_FAMILY_BLOCK)
             fam = family_override;
         else if (n_vec > 32)
             fam = SPMM_FAMILY_WARPROW;   // measured faster than COLTILE on the wide workloads
@@ -423,14 +443,16 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     }
     if (fam == SPMM_FAMILY_COLTILE) lanes = 32;     // one 128-column tile per warp
     o->lanes = (int32_t)lanes;
-    o->col_tiles = fam == SPMM_FAMILY_WINDOW
-                       ? (int32_t)win_tiles
-                       : (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
+    if (fam == SPMM_FAMILY_BLOCK) lanes = 32;
+    o->col_tiles = fam == SPMM_FAMILY_WINDOW  ? (int32_t)win_tiles
+                   : fam == SPMM_FAMILY_BLOCK ? (int32_t)((N + 127) / 128)
+                                              : (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
     o->family = fam;
     o->rows_per_warp = fam == SPMM_FAMILY_ROWGROUP ? (int32_t)(32 / lanes) : 1;
-    o->launches = (d->M > 0 && N > 0) ? 1 + (d->n_heavy > 0 ? 2 : 0) : 0;
+    const bool split = d->n_heavy > 0 && fam != SPMM_FAMILY_BLOCK;
+    o->launches = (d->M > 0 && N > 0) ? 1 + (split ? 2 : 0) : 0;
     const size_t per = (size_t)d->n_chunks * (size_t)N * 4;
-    o->workspace_bytes = d->n_heavy > 0 ? (int64_t)(reduce == SPMM_MAX ? 2 * per : per) : 0;
+    o->workspace_bytes = split ? (int64_t)(reduce == SPMM_MAX ? 2 * per : per) : 0;
 }
 
 }  // namespace spmm
@@ -452,7 +474,7 @@ spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce
                        int num_sms, int family_override, spmm_plan_info *out) {
     if (!desc || !out || N < 0) return SPMM_ERR_INVALID_ARG;
     if (reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
-    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_WINDOW)
+    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_BLOCK)
         return SPMM_ERR_INVALID_ARG;
     route_fill(desc, N, reduce, aligned, num_sms, family_override, out);
     return SPMM_OK;
@@ -547,6 +569,8 @@ static void fill_desc(const Plan *p, spmm_plan_info *o) {
     o->n_heavy = p->n_heavy;
     o->n_chunks = p->n_chunks;
     o->band_w = p->band_w;
+    o->rows_sorted = p->rows_sorted ? 1 : 0;
+    o->blk_intra = p->blk_intra;
     o->band_cover = p->band_cover;
 }
 
@@ -559,7 +583,7 @@ spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce, 
 }
 
 spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split) {
-    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_WINDOW) return SPMM_ERR_INVALID_ARG;
+    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_BLOCK) return SPMM_ERR_INVALID_ARG;
     Plan *p = reinterpret_cast<Plan *>(plan);
     p->family_override = family;
     const int64_t want = t_split > 0 ? t_split : p->t_split_default;
@@ -583,7 +607,7 @@ spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *
     cudaStream_t s = (cudaStream_t)stream;
     int32_t flag = 0;
     unsigned long long *d_hist = nullptr;
-    unsigned long long h_hist[kSpreadBins] = {0};
+    unsigned long long h_hist[kHistWords] = {0};
     cudaError_t e = dev_alloc((void **)&d_hist, sizeof(h_hist));
     if (e == cudaSuccess) e = cudaMemsetAsync(d_hist, 0, sizeof(h_hist), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(p->err + kErrBadCol, 0, sizeof(int32_t), s);
@@ -607,6 +631,8 @@ spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *
         total += h_hist[b];
     }
     p->spread_known = true;
+    p->blk_intra = (int64_t)h_hist[kSpreadBins];
+    p->rows_sorted = h_hist[kSpreadBins + 1] == 0;
     p->band_w = 0;
     p->band_cover = 0.0;
     for (int b = 0; b <= 12 && total > 0; ++b) {
@@ -683,7 +709,9 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
     a.err = p->err;
     a.bias = bias;
     a.act = (int32_t)act;
-    if (p->n_heavy > 0) {
+    a.rows_sorted = p->rows_sorted ? 1 : 0;
+    const bool split = p->n_heavy > 0 && r.family != SPMM_FAMILY_BLOCK;
+    if (split) {
         spmm_status st = ensure_workspace(p, workspace_need(p, N, reduce));
         if (st != SPMM_OK) return st;
         a.ws_val = reinterpret_cast<float *>(p->work);
@@ -694,7 +722,9 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
     }
     const bool has_val = val != nullptr;
     cudaError_t e;
-    if (r.family == SPMM_FAMILY_WINDOW) {
+    if (r.family == SPMM_FAMILY_BLOCK) {
+        e = launch_block(a, reduce, has_val, s);
+    } else if (r.family == SPMM_FAMILY_WINDOW) {
         WinShape w;
         const int rpg = (int)((int64_t)r.window_rows * r.lanes / (kWarp * 16));
         window_shape(p->M, p->K, N, p->dbar, p->band_w, has_val, r.lanes, r.window_chunks, rpg,
@@ -712,7 +742,7 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
         e = launch_rowgroup(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
     else
         e = launch_warprow(a, r.vec, r.lanes, reduce, has_val, r.col_tiles, s);
-    if (e == cudaSuccess && p->n_heavy > 0) {
+    if (e == cudaSuccess && split) {
         // the split rows take the lane shape of the row-per-warp families (the
         // WINDOW family's lanes cover only part of its column tile)
         int64_t hl = r.lanes, ht = r.col_tiles;

@@ -76,6 +76,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     return false;
 }
 
+// One poll without a suspend hint (returns after a short, implementation-defined
+// time); for waits that are expected to end within microseconds.
+__device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// mbar_wait with plain polls, bounded the same way.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t *bar, uint32_t parity, int32_t *err) {
+    if (mbar_poll(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kSpinLimit; ++i) {
+        if (mbar_poll(bar, parity)) return true;
+        if ((i & 255) == 0 && global_ns() - t0 > kWaitLimitNs) break;
+    }
+    atomicOr(err + kErrTimeout, 1);
+    return false;
+}
+
 // Shared-memory loads by 32-bit shared-window address (volatile: they stay
 // after the mbarrier wait that publishes the data).
 __device__ __forceinline__ int lds_s32(uint32_t addr) {

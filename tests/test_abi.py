@@ -158,3 +158,21 @@ def test_router_window_rule(sdm):
     assert r["family_name"] == "window"                                           # pinned
     wide = dict(_desc(cv=0.0), band_w=4096, band_cover=0.9)
     assert sdm.spmm_route(wide, 512, 0)["family_name"] == "warprow"             # ring too big
+
+
+def test_router_block_rule(sdm):
+    # community 64k: 256 blocks of 256 rows, 51 of 56 entries per row inside the block;
+    # BLOCK is used only when pinned (it measured slower than WARPROW there)
+    com = dict(_desc(M=65536, nnz=3668321, cv=0.1), band_w=256, band_cover=0.91,
+               rows_sorted=1, blk_intra=3342000)
+    assert sdm.spmm_route(com, 128, 0)["family_name"] != "block"
+    pin = sdm.FAMILY["block"]
+    r = sdm.spmm_route(com, 128, 0, family=pin)
+    assert (r["family_name"], r["col_tiles"], r["launches"]) == ("block", 1, 1)
+    assert sdm.spmm_route(com, 512, 1, family=pin)["col_tiles"] == 4            # mean too
+    assert sdm.spmm_route(com, 128, 2, family=pin)["family_name"] != "block"   # max
+    assert sdm.spmm_route(com, 40, 0, family=pin)["family_name"] != "block"    # N % 16
+    r = sdm.spmm_route(com, 128, 0, aligned=2, family=pin)
+    assert r["family_name"] != "block"                                          # unaligned B/C
+    r = sdm.spmm_route(dict(com, rows_sorted=0), 128, 0, family=pin)
+    assert r["family_name"] == "block"                                          # any row order
