@@ -223,7 +223,8 @@ spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce
 
 /*
  * spmm_default_t_split -- the heavy-row threshold the plan uses for a graph of
- * `nnz` entries on `num_sms` SMs (pure host function).
+ * `nnz` entries on `num_sms` SMs: nnz / (128 num_sms) clamped to [256, 512]
+ * (pure host function).
  */
 int64_t spmm_default_t_split(int64_t M, int64_t nnz, int num_sms);
 

@@ -122,7 +122,8 @@ def test_router_split_launches_and_workspace(sdm):
 
 def test_default_split_threshold(sdm):
     assert sdm.spmm_default_t_split(2048, 16384, 152) == 256
-    assert sdm.spmm_default_t_split(1 << 22, 104_839_949, 152) == 104_839_949 // (128 * 152)
+    assert sdm.spmm_default_t_split(1 << 22, 104_839_949, 152) == 512
+    assert sdm.spmm_default_t_split(1 << 20, 128 * 152 * 300, 152) == 300
     assert sdm.spmm_default_t_split(10, 10, 0) == 256
 
 
