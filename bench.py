@@ -43,11 +43,11 @@ METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
 # sha256 of the CUDA sources then (kernel_sources_sha256()), and the bench reports
 # traffic as null once the sources differ.
 NCU_TRAFFIC = {
-    "sources_sha256": "5ae1091692d54419a63e3357371111aeaa50a25ec0b820df00de83bf504e3892",
-    "window/knn_1M/N16/sum": 149.16e6,
-    "window/knn_1M/N16/mean": 148.52e6,
-    "window/knn_1M/N64/sum": 557.58e6,
-    "window/knn_1M/N64/mean": 560.45e6,
+    "sources_sha256": "8317a409befddc5319693afbac3ff31eee22c11890dfb421d539d68ea89b53e1",
+    "window/knn_1M/N16/sum": 148.99e6,
+    "window/knn_1M/N16/mean": 149.13e6,
+    "window/knn_1M/N64/sum": 557.73e6,
+    "window/knn_1M/N64/mean": 560.46e6,
 }
 
 

@@ -151,7 +151,8 @@ struct WinLane {
     }
 };
 
-template <int L, int Q, int RED, bool HAS_VAL, bool CHECK, bool POW2>
+// EPI: the fused bias/ReLU epilogue is compiled in only where it is used
+template <int L, int Q, int RED, bool HAS_VAL, bool CHECK, bool POW2, bool EPI>
 __global__ void __launch_bounds__(kWinThreads, 1)
     k_window(const RunArgs a, const WinShape w, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(kWinThreads, 1)
             float out[4];
             int arg[4];
             acc[k].finish(d, out, arg);
-            epilogue<4>(a, cq[k], out);
+            if constexpr (EPI) epilogue<4>(a, cq[k], out);
             st_vec<4>(a.C + i * N + cq[k], out);
             if (RED == SPMM_MAX && a.argmax) st_vec_i<4>(a.argmax + i * N + cq[k], arg);
         }
@@ -444,8 +445,11 @@ namespace window_detail {
 template <int L, int Q, int RED, bool HAS_VAL, bool CHECK>
 cudaError_t go(const RunArgs &a, const WinShape &w, const CUtensorMap &map, int grid_x, int tiles,
                cudaStream_t s) {
-    auto kern = w.pow2 ? k_window<L, Q, RED, HAS_VAL, CHECK, true>
-                       : k_window<L, Q, RED, HAS_VAL, CHECK, false>;
+    const bool epi = a.bias != nullptr || a.act != SPMM_ACT_NONE;
+    auto kern = w.pow2 ? (epi ? k_window<L, Q, RED, HAS_VAL, CHECK, true, true>
+                              : k_window<L, Q, RED, HAS_VAL, CHECK, true, false>)
+                       : (epi ? k_window<L, Q, RED, HAS_VAL, CHECK, false, true>
+                              : k_window<L, Q, RED, HAS_VAL, CHECK, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          w.smem_bytes);
     if (e != cudaSuccess) return e;
