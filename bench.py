@@ -71,7 +71,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--family", default="auto", choices=["auto", "rowgroup", "warprow", "coltile"])
+    ap.add_argument("--family", default="auto",
+                    choices=["auto", "rowgroup", "warprow", "coltile", "window", "block"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
