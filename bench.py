@@ -74,8 +74,20 @@ def parse():
     ap.add_argument("--family", default="auto",
                     choices=["auto", "rowgroup", "warprow", "coltile", "window", "block"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=120.0,
+                    help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
+
+
+def max_over_ranks(x: float, pg, device=None) -> float:
+    """The largest value of x over the ranks (x itself without a process group)."""
+    if pg is None:
+        return float(x)
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
 
 
 def dist_init(args):
@@ -230,7 +242,7 @@ def run_reference(args):
     import gen
     B_by_N = {n: gen.features(g.K, n, seed=0) for n in spec["N"]}
     # each step: a row sample sized so that W + K steps end within ~2 minutes
-    budget_total = 120.0
+    budget_total = args.ref_budget
     per_step = budget_total / max(1, args.steps + args.warmup)
     import oracle
     probe_rows, _ = sample_rows(g, min(1.0, 2000 / max(g.M, 1)), seed=1)
@@ -352,9 +364,7 @@ def run_ours(args):
     per_run_ms = np.array([[a.elapsed_time(b) for a, b in ev[s]] for s in range(args.steps)])
     dev_ms = float(per_run_ms.sum())
     if pg is not None:
-        t = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        dev_ms = float(t.item())
+        dev_ms = max_over_ranks(dev_ms, pg, dev)
     flops_step = sum(2.0 * g.nnz * n for n, _ in runs)
     value = flops_step * args.steps * world / (dev_ms / 1e3) / 1e9
 
