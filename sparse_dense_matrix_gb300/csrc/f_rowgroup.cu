@@ -50,12 +50,32 @@ __global__ void __launch_bounds__(256) k_rowgroup(const RunArgs a) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) acc.add(w[u], j[u], b[u]);
     }
-    for (; p < p1; ++p) {
-        const int j = ld_stream(a.col + p);
-        const float w = HAS_VAL ? ld_stream(a.val + p) : 1.0f;
-        float b[V];
-        ld_vec<V>(Bv + (int64_t)j * N, b);
-        acc.add(w, j, b);
+    // the last (< 4) entries: for the sum with narrow rows of lanes their
+    // loads are issued together, predicated (one round trip); the order of
+    // the adds is the same either way
+    if constexpr (RED == SPMM_SUM && L <= 16) {
+        int j[3];
+        float w[3], b[3][V];
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const bool in = p + u < p1;
+            j[u] = in ? ld_stream(a.col + p + u) : 0;
+            w[u] = (HAS_VAL && in) ? ld_stream(a.val + p + u) : 1.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 3; ++u)
+            if (p + u < p1) ld_vec<V>(Bv + (int64_t)j[u] * N, b[u]);
+#pragma unroll
+        for (int u = 0; u < 3; ++u)
+            if (p + u < p1) acc.add(w[u], j[u], b[u]);
+    } else {
+        for (; p < p1; ++p) {
+            const int j = ld_stream(a.col + p);
+            const float w = HAS_VAL ? ld_stream(a.val + p) : 1.0f;
+            float b[V];
+            ld_vec<V>(Bv + (int64_t)j * N, b);
+            acc.add(w, j, b);
+        }
     }
     if (vi >= a.n_vec) return;
     float out[V];
