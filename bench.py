@@ -40,10 +40,10 @@ METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # `ncu --set full` capture of the bench step (profiles/window_knn1M_bench.md). The
 # counters belong to the kernel build they were taken on: "sources_sha256" is the
-# sha256 of the CUDA sources then (kernel_sources_sha256()), and the bench reports
-# traffic as null once the sources differ.
+# sha256 of the WINDOW kernel's sources then (kernel_sources_sha256()), and the
+# bench reports traffic as null once they differ.
 NCU_TRAFFIC = {
-    "sources_sha256": "8317a409befddc5319693afbac3ff31eee22c11890dfb421d539d68ea89b53e1",
+    "sources_sha256": "01346a8910aca124d21ca6d8a9a79f87603b0cd94462c7707d68ab09aae52f98",
     "window/knn_1M/N16/sum": 148.99e6,
     "window/knn_1M/N16/mean": 149.13e6,
     "window/knn_1M/N64/sum": 557.73e6,
@@ -51,14 +51,20 @@ NCU_TRAFFIC = {
 }
 
 
+# the sources the WINDOW kernel (the bench's dominant kernel) is built from
+WINDOW_SOURCES = ("sparse_dense_matrix_gb300/csrc/common.cuh", "sparse_dense_matrix_gb300/csrc/tma.cuh",
+                  "sparse_dense_matrix_gb300/csrc/window.cuh", "sparse_dense_matrix_gb300/csrc/f_window.cu",
+                  "sparse_dense_matrix_gb300/csrc/f_window_sum.cu",
+                  "sparse_dense_matrix_gb300/csrc/f_window_mean.cu",
+                  "sparse_dense_matrix_gb300/csrc/f_window_max.cu", "include/spmm.h")
+
+
 def kernel_sources_sha256():
-    csrc = os.path.join(ROOT, "sparse_dense_matrix_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            h.update(name.encode())
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for rel in WINDOW_SOURCES:
+        h.update(rel.encode())
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()
 
 FALLBACK_HBM_GBS = 6800.0
