@@ -100,6 +100,7 @@ struct RunArgs {
     const float *__restrict__ bias;           // [N] added to every output row, or NULL
     int32_t act;                              // spmm_activation applied after the bias
     int32_t rows_sorted;                      // columns non-decreasing within every row
+    int32_t mean;                             // 1: a SUM kernel finishes the mean (x 1/d)
 };
 
 // Fused epilogue on V consecutive outputs starting at column c: C = act(C + bias)
@@ -236,6 +237,17 @@ struct Acc {
         }
     }
 };
+
+// The mean finished by a SUM kernel (the row-per-warp families run the mean as
+// the sum plus this step): fl(S * rcp(d)) as Acc<..., MEAN>::finish, 0 for d = 0.
+template <int V>
+__device__ __forceinline__ void mean_scale(const RunArgs &a, int d, float (&out)[V]) {
+    if (a.mean) {
+        const float inv_d = d > 0 ? rcp_approx((float)d) : 0.0f;
+#pragma unroll
+        for (int e = 0; e < V; ++e) out[e] = __fmul_rn(out[e], inv_d);
+    }
+}
 
 // Number of kernels launched by this library (spmm_launch_count).
 extern std::atomic<uint64_t> g_launches;

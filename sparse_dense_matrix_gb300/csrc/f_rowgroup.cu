@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(256) k_rowgroup(const RunArgs a) {
     float out[V];
     int arg[V];
     acc.finish(d, out, arg);
+    if constexpr (RED == SPMM_SUM) mean_scale<V>(a, d, out);
     epilogue<V>(a, (int64_t)vi * V, out);
     st_vec<V>(a.C + row * N + (int64_t)vi * V, out);
     if (RED == SPMM_MAX && a.argmax) st_vec_i<V>(a.argmax + row * N + (int64_t)vi * V, arg);
@@ -121,7 +122,14 @@ cudaError_t by_reduce(const RunArgs &a, int reduce, bool has_val, int lanes, int
                       cudaStream_t s) {
     switch (reduce) {
         case SPMM_SUM: return by_val<V, SPMM_SUM>(a, has_val, lanes, tiles, s);
-        case SPMM_MEAN: return by_val<V, SPMM_MEAN>(a, has_val, lanes, tiles, s);
+        case SPMM_MEAN:
+            if (lanes == 32) {
+                // whole-warp rows: the mean as the sum with a final 1/d (as in WARPROW)
+                RunArgs m = a;
+                m.mean = 1;
+                return by_val<V, SPMM_SUM>(m, has_val, lanes, tiles, s);
+            }
+            return by_val<V, SPMM_MEAN>(a, has_val, lanes, tiles, s);
         case SPMM_MAX: return by_val<V, SPMM_MAX>(a, has_val, lanes, tiles, s);
         default: return cudaErrorInvalidValue;
     }
