@@ -311,6 +311,18 @@ spmm_status spmm_maxpool_backward(spmm_plan_t planT, const int32_t *colT, const 
                                   const int32_t *argmax, const float *dC, int64_t N, float *dB,
                                   void *stream);
 
+/*
+ * spmm_check_wait_timeout -- diagnostic of the failure path. Every spin-wait in
+ * the library's kernels is bounded: when it gives up it records a timeout in
+ * the plan's error words and the kernel returns (no trap), and
+ * spmm_plan_sync then reports SPMM_ERR_TIMEOUT. This call runs, on `stream`,
+ * one kernel whose wait nothing completes, with a limit of `limit_us`
+ * microseconds (1 .. 10^7), then returns what spmm_plan_sync returns:
+ * SPMM_ERR_TIMEOUT when the path works. The plan and the CUDA context stay
+ * usable afterwards. Synchronous.
+ */
+spmm_status spmm_check_wait_timeout(spmm_plan_t plan, int64_t limit_us, void *stream);
+
 /* spmm_plan_destroy -- free the plan and everything it owns. NULL is a no-op. */
 spmm_status spmm_plan_destroy(spmm_plan_t plan);
 

@@ -31,6 +31,7 @@ __all__ = [
     "spmm_plan_reserve", "spmm_plan_validate_cols", "spmm_plan_sync", "spmm_plan_set_family",
     "spmm_route", "spmm_default_t_split", "spmm_status_string", "spmm_launch_count",
     "spmm_run_noalloc", "spmm_transpose", "spmm_maxpool_backward", "spmm_run_ex", "ACT",
+    "spmm_check_wait_timeout",
     "PlanInfo", "REDUCE", "FAMILY", "lib", "build_library",
 ]
 
@@ -95,6 +96,7 @@ def _load():
         "spmm_launch_count": ([], ctypes.c_uint64),
         "spmm_run_noalloc": ([vp, vp, vp, vp, i64, i64, i64, i32, vp, vp, vp], i32),
         "spmm_transpose": ([vp, vp, vp, i32, vp, vp, vp, vp], i32),
+        "spmm_check_wait_timeout": ([vp, i64, vp], i32),
         "spmm_maxpool_backward": ([vp, vp, vp, vp, vp, i64, vp, vp], i32),
     }
     for name, (args, res) in sigs.items():
@@ -209,6 +211,11 @@ def spmm_transpose(plan: int, col_ptr, val_ptr, scale_mean: bool, rowptrT_ptr: i
     """A^T in CSR (synchronous; see include/spmm.h)."""
     _check(lib.spmm_transpose(plan, col_ptr, val_ptr, 1 if scale_mean else 0, rowptrT_ptr,
                               colT_ptr, valT_ptr, _stream_handle(stream)), "spmm_transpose")
+
+
+def spmm_check_wait_timeout(plan: int, limit_us: int, stream=None) -> int:
+    """Run one bounded wait that nothing completes; returns the status (6 = timeout)."""
+    return int(lib.spmm_check_wait_timeout(plan, limit_us, _stream_handle(stream)))
 
 
 def spmm_maxpool_backward(planT: int, colT_ptr, valT_ptr, argmax_ptr, dC_ptr, N: int, dB_ptr: int,

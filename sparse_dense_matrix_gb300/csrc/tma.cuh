@@ -65,12 +65,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 
 // Wait for phase `parity` of `bar` to complete; false (and the error word set)
 // if it has not within the limits above.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255) == 0 && global_ns() - t0 > kWaitLimitNs) break;
+        if ((i & 255) == 0 && global_ns() - t0 > limit_ns) break;
     }
     atomicOr(err + kErrTimeout, 1);
     return false;

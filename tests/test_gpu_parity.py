@@ -365,3 +365,17 @@ def test_window_family_community_and_unaligned_col(sdm, cuda_device):
     adj2.set_family("window")
     C, A = gpu_reduce(adj2, Bd, "sum")
     compare(g, B, "sum", C, A, label="window unaligned col")
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(sdm, cuda_device):
+    """A wait that nothing completes gives up after its limit: the plan reports
+    SPMM_ERR_TIMEOUT (6), the error words are cleared, and the plan and the
+    context keep working."""
+    g = small("er")
+    adj = make_adj(sdm, g, cuda_device)
+    assert sdm.spmm_check_wait_timeout(adj.plan, 2000) == 6
+    sdm.spmm_plan_sync(adj.plan)                    # cleared: no error left behind
+    B = gen.features(g.K, 16, seed=1)
+    C, A = gpu_reduce(adj, to_dev(B, cuda_device), "sum")
+    compare(g, B, "sum", C, A, label="after a timeout")
+    adj.close()
