@@ -154,9 +154,11 @@ spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, con
                      int64_t N, spmm_reduce reduce, float *C, int32_t *argmax, void *stream);
 
 /*
- * spmm_run_ex -- spmm_run with a fused epilogue on every output element
- * (GraphSPMM, "SpMM fused with the layer's epilogue": the bias and the
- * activation are applied where C is written, so C makes one trip to memory):
+ * spmm_run_ex -- spmm_run with a fused epilogue on every output element. A GCN
+ * layer is the aggregation SpMM followed by the node update ("Dual-Metric
+ * Partitioning with Adaptive Kernel Execution for Efficient GCN Acceleration",
+ * introduction); here the bias and the activation are applied where C is
+ * written, so C makes one trip to memory:
  *   C[i,k] = act(R[i,k] + bias[k])
  * with R the reduction's value as spmm_run defines it (empty rows included:
  * R = 0), the addition in fp32 (round to nearest) and act applied after it.

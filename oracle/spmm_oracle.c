@@ -33,7 +33,9 @@
  *   T[i,k] = sum_p |x_p| is returned beside sum/mean as the scale of the
  *   floating-point tolerance |err| <= 1e-5 * T + 1e-6.
  *
- * Epilogue (GraphSPMM: the SpMM fused with the layer's bias and activation):
+ * Epilogue (a GCN layer's aggregation followed by its node update, "Dual-Metric
+ * Partitioning with Adaptive Kernel Execution for Efficient GCN Acceleration",
+ * introduction; here the bias and activation of that update):
  *   with a bias vector b [N] and/or ReLU, the output is
  *   act(R[i,k] + b[k]) where R is the value defined above before its final
  *   rounding (the fp64 sum, or the fp64 mean, or the fp32 max), the addition

@@ -103,9 +103,12 @@ struct RunArgs {
     int32_t mean;                             // 1: a SUM kernel finishes the mean (x 1/d)
 };
 
-// Fused epilogue on V consecutive outputs starting at column c: C = act(C + bias)
-// (GraphSPMM-style "SpMM followed by an epilogue"; the argmax of max is not
-// affected). ReLU is x > 0 ? x : +0, so -0 and negative values give +0.
+// Fused epilogue on V consecutive outputs starting at column c: C = act(C + bias).
+// A GCN layer is the aggregation SpMM followed by the node update ("Dual-Metric
+// Partitioning with Adaptive Kernel Execution for Efficient GCN Acceleration",
+// introduction); applying the bias and activation where C is written saves C a
+// round trip. The argmax of max is not affected. ReLU is x > 0 ? x : +0, so -0
+// and negative values give +0.
 template <int V>
 __device__ __forceinline__ void epilogue(const RunArgs &a, int64_t c, float (&out)[V]) {
     if (a.bias) {
