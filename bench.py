@@ -43,11 +43,11 @@ METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
 # sha256 of the WINDOW kernel's sources then (kernel_sources_sha256()), and the
 # bench reports traffic as null once they differ.
 NCU_TRAFFIC = {
-    "sources_sha256": "cb2804e1299e2cc872b6f969a5040ce99f6fe5932136cf2d2d225996165c84c1",
-    "window/knn_1M/N16/sum": 149.02e6,
-    "window/knn_1M/N16/mean": 148.54e6,
-    "window/knn_1M/N64/sum": 557.73e6,
-    "window/knn_1M/N64/mean": 560.54e6,
+    "sources_sha256": "4b8d95cf0b86d716ae7754b6eabb57fa1a6e665c926bdc6a296ceb24015c4ef3",
+    "window/knn_1M/N16/sum": 148.96e6,
+    "window/knn_1M/N16/mean": 148.77e6,
+    "window/knn_1M/N64/sum": 557.94e6,
+    "window/knn_1M/N64/mean": 561.01e6,
 }
 
 
