@@ -43,11 +43,11 @@ METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
 # sha256 of the WINDOW kernel's sources then (kernel_sources_sha256()), and the
 # bench reports traffic as null once they differ.
 NCU_TRAFFIC = {
-    "sources_sha256": "4b8d95cf0b86d716ae7754b6eabb57fa1a6e665c926bdc6a296ceb24015c4ef3",
-    "window/knn_1M/N16/sum": 148.96e6,
-    "window/knn_1M/N16/mean": 148.77e6,
-    "window/knn_1M/N64/sum": 557.94e6,
-    "window/knn_1M/N64/mean": 561.01e6,
+    "sources_sha256": "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af",
+    "window/knn_1M/N16/sum": 149.09e6,
+    "window/knn_1M/N16/mean": 148.67e6,
+    "window/knn_1M/N64/sum": 557.30e6,
+    "window/knn_1M/N64/mean": 559.95e6,
 }
 
 
@@ -83,6 +83,12 @@ def parse():
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--n", default=None,
+                    help="comma-separated feature widths to run (default: all of the workload's)")
+    ap.add_argument("--reduce", default=None,
+                    help="comma-separated reductions to run (default: all of the workload's)")
+    ap.add_argument("--warm-iters", type=int, default=20,
+                    help="back-to-back launches per run for the warm-L2 figure (0: skip)")
     return ap.parse_args()
 
 
@@ -119,11 +125,20 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload(cid):
+def workload(cid, n_sel=None, r_sel=None):
+    """The workload's generator spec, its graph and the (N, reduce) runs of one
+    step; n_sel / r_sel restrict the runs to a comma-separated subset."""
     import gen
     spec = gen.CONFIGS[cid]
+    Ns = spec["N"] if n_sel is None else [int(x) for x in n_sel.split(",")]
+    Rs = spec["reduce"] if r_sel is None else r_sel.split(",")
+    bad = [n for n in Ns if n not in spec["N"]] + [r for r in Rs if r not in spec["reduce"]]
+    if bad:
+        raise SystemExit(f"--n/--reduce: {bad} not in {spec['name']} "
+                         f"(N {spec['N']}, reduce {spec['reduce']})")
     g = gen.config(cid)
-    runs = [(n, r) for n in spec["N"] for r in spec["reduce"]]
+    runs = [(n, r) for n in Ns for r in Rs]
+    spec = dict(spec, N=Ns, reduce=Rs)
     return spec, g, runs
 
 
@@ -244,7 +259,7 @@ def run_reference(args):
     world, rank, _, pg = dist_init(args)
     if rank != 0:
         return
-    spec, g, runs = workload(args.config)
+    spec, g, runs = workload(args.config, args.n, args.reduce)
     import gen
     B_by_N = {n: gen.features(g.K, n, seed=0) for n in spec["N"]}
     # each step: a row sample sized so that W + K steps end within ~2 minutes
@@ -288,7 +303,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     import sparse_dense_matrix_gb300 as sdm
 
-    spec, g, runs = workload(args.config)
+    spec, g, runs = workload(args.config, args.n, args.reduce)
     import gen
     Ns = spec["N"]
     B_host = {n: gen.features(g.K, n, seed=0) for n in Ns}
@@ -367,6 +382,23 @@ def run_ours(args):
     sdm.spmm_plan_sync(adj.plan)
     clk = clocks.stop(t0, t1)
 
+    # Warm-L2 figure, outside the timed region and not part of value: each run
+    # launched back to back without the flush, so B, col and C stay in L2 as far
+    # as they fit.
+    warm_ms = [None] * len(runs)
+    if args.warm_iters > 0:
+        wev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.warm_iters)] for _ in runs]
+        for k, (n, r) in enumerate(runs):
+            one(n, r)
+            for a, b in wev[k]:
+                a.record(stream)
+                one(n, r)
+                b.record(stream)
+        torch.cuda.synchronize()
+        warm_ms = [float(np.median([a.elapsed_time(b) for a, b in wev[k]]))
+                   for k in range(len(runs))]
+
     per_run_ms = np.array([[a.elapsed_time(b) for a, b in ev[s]] for s in range(args.steps)])
     dev_ms = float(per_run_ms.sum())
     if pg is not None:
@@ -395,6 +427,9 @@ def run_ours(args):
         b = compulsory_bytes(g, n, r)
         per_run.append({"N": n, "reduce": r, "family": adj.describe(n, r)["family_name"],
                         "ms": float(np.median(per_run_ms[:, k])),
+                        "ms_p10": float(np.percentile(per_run_ms[:, k], 10)),
+                        "ms_p90": float(np.percentile(per_run_ms[:, k], 90)),
+                        "warm_l2_ms": warm_ms[k],
                         "gflops": 2.0 * g.nnz * n / (np.median(per_run_ms[:, k]) / 1e3) / 1e9,
                         "hbm_frac": b / (np.median(per_run_ms[:, k]) / 1e3) / 1e9 / hbm_peak})
 
@@ -481,7 +516,10 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": describe_workload(spec, g, runs),
                        "l2": "flushed (write of 2x L2) before every timed launch",
-                       "timing": "CUDA events around each spmm_run on the launching stream",
+                       "timing": "CUDA events around each spmm_run on the launching stream; "
+                                 "per_run ms is the median over steps, with p10 and p90",
+                       "warm_l2": "per_run warm_l2_ms: back-to-back launches without the "
+                                  "flush, after the timed region; not part of value",
                        "per_run": per_run},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clk, "cold_path": cold,
