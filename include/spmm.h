@@ -110,6 +110,8 @@ typedef struct {
     /* block structure, known after spmm_plan_validate_cols (0 before) */
     int32_t rows_sorted;    /* 1 if every row's columns are non-decreasing             */
     int64_t blk_intra;      /* entries with col / 256 == row / 256 (diagonal blocks)     */
+    /* row-range plans (spmm_plan_create_range): global index of the plan's row 0 */
+    int64_t row0;
 } spmm_plan_info;
 
 /*
@@ -128,6 +130,53 @@ typedef struct {
  */
 spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *stream,
                              spmm_plan_t *out);
+
+/*
+ * spmm_plan_create_range -- a plan for the contiguous rows [row_begin, row_end)
+ * of a larger CSR matrix: one worker's share when rows are split across
+ * workers (each row's output depends on that row alone, so the shares need no
+ * exchange). Built like spmm_plan_create over those rows.
+ *   rowptr    : device (or host), int32 [>= row_end + 1], the WHOLE matrix's
+ *               row pointers; entries row_begin .. row_end are copied and
+ *               rebased to start at 0. rowptr[0] itself need not be read.
+ *   row_begin, row_end : 0 <= row_begin <= row_end < 2^31.
+ *   K, stream, out : as in spmm_plan_create. Synchronous.
+ * The plan's rows are local: M = row_end - row_begin, and C / argmax passed to
+ * spmm_run are [M, N]. col and val passed to spmm_run, spmm_run_ex,
+ * spmm_plan_validate_cols and spmm_transpose are the WHOLE matrix's arrays
+ * (the plan reads its rows' entries from offset rowptr[row_begin]); B is the
+ * whole K x N matrix. Column locality is measured against the global row, so
+ * a banded matrix keeps its banded routing when the range starts on a
+ * multiple of the WINDOW family's tile rows (256 covers every tile shape);
+ * the BLOCK family needs row_begin == 0. Returns SPMM_ERR_INVALID_INPUT when
+ * the copied entries decrease or rowptr[row_begin] < 0.
+ */
+spmm_status spmm_plan_create_range(const int32_t *rowptr, int64_t row_begin, int64_t row_end,
+                                   int64_t K, void *stream, spmm_plan_t *out);
+
+/*
+ * spmm_partition_rows -- contiguous row ranges for `parts` workers, balanced
+ * by work (pure host code; no CUDA call).
+ *   rowptr     : HOST, int32 [M+1], a CSR row-pointer array (rowptr[0] == 0,
+ *                non-decreasing; checked, SPMM_ERR_INVALID_INPUT otherwise).
+ *   M          : rows, 0 <= M < 2^31.
+ *   parts      : workers, >= 1.
+ *   align_rows : every inner bound is a multiple of this (>= 1; 256 keeps
+ *                banded ranges eligible for the WINDOW family).
+ *   bounds     : HOST, int64 [parts + 1], receives 0 = b_0 <= b_1 <= ... <=
+ *                b_parts = M; worker q owns rows [b_q, b_{q+1}).
+ * A row's work is its entry count plus one (its output row). Bound q is the
+ * first row whose prefix work reaches q/parts of the total, rounded to the
+ * nearest multiple of align_rows and kept in order, so no row is split and a
+ * heavy row stays whole on one worker. The objective is the block-workload
+ * balance (maximum over average block work) of "Dual-Metric Partitioning with
+ * Adaptive Kernel Execution for Efficient GCN Acceleration", section
+ * "Adaptive Data Partitioning", with row degree as the width metric; its
+ * random-walk density term and its reordering of nodes are not used, so each
+ * worker's rows stay contiguous and C needs no permutation.
+ */
+spmm_status spmm_partition_rows(const int32_t *rowptr, int64_t M, int32_t parts,
+                                int64_t align_rows, int64_t *bounds);
 
 /*
  * spmm_run -- C = reduce_j A[i,j] * B[j,:] for every row i (asynchronous).

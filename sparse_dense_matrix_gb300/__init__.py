@@ -31,7 +31,7 @@ __all__ = [
     "spmm_plan_reserve", "spmm_plan_validate_cols", "spmm_plan_sync", "spmm_plan_set_family",
     "spmm_route", "spmm_default_t_split", "spmm_status_string", "spmm_launch_count",
     "spmm_run_noalloc", "spmm_transpose", "spmm_maxpool_backward", "spmm_run_ex", "ACT",
-    "spmm_check_wait_timeout",
+    "spmm_check_wait_timeout", "spmm_plan_create_range", "spmm_partition_rows",
     "PlanInfo", "REDUCE", "FAMILY", "lib", "build_library",
 ]
 
@@ -57,6 +57,7 @@ class PlanInfo(ctypes.Structure):
         ("window_rows", ctypes.c_int32), ("window_ctas", ctypes.c_int32),
         ("window_smem", ctypes.c_int64), ("window_chunks", ctypes.c_int32),
         ("rows_sorted", ctypes.c_int32), ("blk_intra", ctypes.c_int64),
+        ("row0", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
@@ -82,6 +83,8 @@ def _load():
     P = ctypes.POINTER
     sigs = {
         "spmm_plan_create": ([vp, i64, i64, vp, P(vp)], i32),
+        "spmm_plan_create_range": ([vp, i64, i64, i64, vp, P(vp)], i32),
+        "spmm_partition_rows": ([vp, i64, i32, i64, P(ctypes.c_int64)], i32),
         "spmm_run": ([vp, vp, vp, vp, i64, i32, vp, vp, vp], i32),
         "spmm_run_ex": ([vp, vp, vp, vp, i64, i32, vp, i32, vp, vp, vp], i32),
         "spmm_plan_reserve": ([vp, i64, i32], i32),
@@ -132,6 +135,33 @@ def spmm_launch_count() -> int:
 
 def spmm_default_t_split(M: int, nnz: int, num_sms: int) -> int:
     return int(lib.spmm_default_t_split(M, nnz, num_sms))
+
+
+def spmm_plan_create_range(rowptr_ptr: int, row_begin: int, row_end: int, K: int,
+                           stream=None) -> int:
+    """Plan for rows [row_begin, row_end) of the matrix whose whole rowptr is given."""
+    out = ctypes.c_void_p()
+    _check(lib.spmm_plan_create_range(rowptr_ptr, row_begin, row_end, K, _stream_handle(stream),
+                                      ctypes.byref(out)), "spmm_plan_create_range")
+    return out.value
+
+
+def spmm_partition_rows(rowptr, parts: int, align_rows: int = 1) -> list:
+    """Row bounds [b_0 = 0, ..., b_parts = M] of `parts` contiguous ranges balanced
+    by entries + rows. ``rowptr``: a host array (numpy or CPU tensor; a CUDA
+    tensor is copied to the host first)."""
+    import numpy as np
+    if hasattr(rowptr, "detach"):
+        rowptr = rowptr.detach().cpu().numpy()
+    rp = np.ascontiguousarray(rowptr, dtype=np.int32)
+    if rp.ndim != 1 or rp.size < 1:
+        raise ValueError("rowptr must be a 1-D array of M+1 entries")
+    if parts < 1:
+        raise ValueError("parts must be >= 1")
+    bounds = (ctypes.c_int64 * (parts + 1))()
+    _check(lib.spmm_partition_rows(rp.ctypes.data, rp.size - 1, parts, align_rows, bounds),
+           "spmm_partition_rows")
+    return [int(b) for b in bounds]
 
 
 def spmm_plan_create(rowptr_ptr: int, M: int, K: int, stream=None) -> int:
@@ -190,7 +220,8 @@ def spmm_route(desc: dict, N: int, reduce: int, aligned: int = 3, num_sms: int =
     """
     d = PlanInfo()
     for k in ("M", "K", "nnz", "d_max", "n_empty", "dbar", "cv", "t_split", "chunk",
-              "n_heavy", "n_chunks", "band_w", "band_cover", "rows_sorted", "blk_intra"):
+              "n_heavy", "n_chunks", "band_w", "band_cover", "rows_sorted", "blk_intra",
+              "row0"):
         if k in desc:
             setattr(d, k, desc[k])
     out = PlanInfo()
@@ -245,7 +276,9 @@ class SparseAdj:
     """A CSR adjacency held once (one plan) and applied many times."""
 
     def __init__(self, rowptr, col, val=None, num_cols: int | None = None,
-                 validate: bool = True):
+                 validate: bool = True, rows: tuple | None = None):
+        """``rows=(b, e)`` builds the product for rows [b, e) only: rowptr, col
+        and val are the whole matrix's, and outputs have e - b rows."""
         import torch
         _req(rowptr, torch.int32, "rowptr")
         dev = rowptr.device
@@ -255,19 +288,30 @@ class SparseAdj:
             if val.numel() != col.numel():
                 raise ValueError("val and col differ in length")
         self.device = dev
-        self.M = rowptr.numel() - 1
-        if self.M < 0:
+        M_all = rowptr.numel() - 1
+        if M_all < 0:
             raise ValueError("rowptr must hold M+1 entries")
-        self.K = int(num_cols) if num_cols is not None else self.M
+        self.rows = (0, M_all) if rows is None else (int(rows[0]), int(rows[1]))
+        if not 0 <= self.rows[0] <= self.rows[1] <= M_all:
+            raise ValueError(f"rows {rows} outside [0, {M_all}]")
+        self.M = self.rows[1] - self.rows[0]
+        self.K = int(num_cols) if num_cols is not None else M_all
         self.rowptr, self.col, self.val = rowptr, col, val
         self._plan = None
         self._t = self._tmean = None
         with torch.cuda.device(dev):
-            self._plan = spmm_plan_create(rowptr.data_ptr(), self.M, self.K)
+            if rows is None:
+                self._plan = spmm_plan_create(rowptr.data_ptr(), self.M, self.K)
+            else:
+                self._plan = spmm_plan_create_range(rowptr.data_ptr(), self.rows[0], self.rows[1],
+                                                    self.K)
             info = spmm_plan_describe(self._plan, 0, 0)
-            if info["nnz"] != col.numel():
+            self.nnz = info["nnz"]
+            if (rows is None and self.nnz != col.numel()) or \
+                    (rows is not None and int(rowptr[self.rows[1]]) > col.numel()):
                 self.close()
-                raise ValueError(f"rowptr[M] = {info['nnz']} but col holds {col.numel()} entries")
+                raise ValueError(f"rowptr holds {self.nnz} entries for these rows but col "
+                                 f"holds {col.numel()}")
             if validate:
                 try:
                     spmm_plan_validate_cols(self._plan, col.data_ptr())
@@ -343,7 +387,7 @@ class SparseAdj:
         (i, j) is a_ij / d_i, so that ``adj.transpose(True) @ dC`` is the
         gradient of ``adj.reduce(B, "mean")`` with respect to B."""
         import torch
-        nnz = self.col.numel()
+        nnz = self.nnz
         rowptrT = torch.empty(self.K + 1, dtype=torch.int32, device=self.device)
         colT = torch.empty(nnz, dtype=torch.int32, device=self.device)
         valT = (torch.empty(nnz, dtype=torch.float32, device=self.device)

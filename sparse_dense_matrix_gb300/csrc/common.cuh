@@ -27,6 +27,11 @@ struct Plan {
 
     int32_t *rowptr = nullptr;       // plan copy of rowptr [M+1], then kRowptrPad copies of rowptr[M]
 
+    // A row-range plan (spmm_plan_create_range) covers rows [row0, row0 + M)
+    // of a larger matrix: its rowptr copy is rebased to start at 0, and the
+    // caller's full col/val arrays are read from entry col_base = rowptr[row0].
+    int64_t row0 = 0, col_base = 0;
+
     // heavy rows (d > t_split): ids ascending, chunk table (row, begin) per
     // chunk of `chunk` entries, first chunk of each heavy row (prefix, n_heavy+1)
     int64_t t_split = 0, t_split_default = 0;
@@ -101,6 +106,8 @@ struct RunArgs {
     int32_t act;                              // spmm_activation applied after the bias
     int32_t rows_sorted;                      // columns non-decreasing within every row
     int32_t mean;                             // 1: a SUM kernel finishes the mean (x 1/d)
+    int64_t row0;                             // global index of local row 0 (row-range plans);
+                                              // only the WINDOW family's column window uses it
 };
 
 // Fused epilogue on V consecutive outputs starting at column c: C = act(C + bias).

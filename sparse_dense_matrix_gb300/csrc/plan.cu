@@ -68,6 +68,14 @@ __device__ __forceinline__ int warp_max_i(int x) {
     return x;
 }
 
+// A row-range plan's copy of rowptr starts at the range's first entry:
+// subtract it so that the copy is a CSR row-pointer array of its own.
+__global__ void k_rebase(int32_t *__restrict__ rp, int64_t n, int32_t base) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        rp[i] -= base;
+}
+
 // Block b summarises rows [b*R, (b+1)*R): degree sums, max, empty rows,
 // decreasing row pointers, rows above t_split.
 __global__ void __launch_bounds__(kDescThreads) k_desc(const int32_t *__restrict__ rowptr,
@@ -160,9 +168,12 @@ constexpr int kSpreadBins = 34;
 // block of kBlockRows x kBlockRows (col / kBlockRows == row / kBlockRows), and
 // entries whose column is below the previous entry's in the same row
 constexpr int kHistWords = kSpreadBins + 2;
+// Rows are local to the plan; the spread and the diagonal blocks are measured
+// against the global row (row + row0) that a row-range plan's row stands for.
 __global__ void __launch_bounds__(256) k_check_cols(const int32_t *__restrict__ rowptr,
                                                    const int32_t *__restrict__ col, int64_t M,
-                                                   int64_t K, int32_t *__restrict__ err,
+                                                   int64_t K, int64_t row0,
+                                                   int32_t *__restrict__ err,
                                                    unsigned long long *__restrict__ hist) {
     __shared__ unsigned int sh[kHistWords];
     for (int b = threadIdx.x; b < kHistWords; b += blockDim.x) sh[b] = 0;
@@ -183,10 +194,11 @@ __global__ void __launch_bounds__(256) k_check_cols(const int32_t *__restrict__ 
                 if (c < 0 || (int64_t)c >= K) {
                     bad = 1;
                 } else {
+                    const int64_t g = row + row0;
                     const unsigned long long dist =
-                        (unsigned long long)((int64_t)c > row ? (int64_t)c - row : row - (int64_t)c);
+                        (unsigned long long)((int64_t)c > g ? (int64_t)c - g : g - (int64_t)c);
                     b = dist <= 1 ? 0 : 64 - __clzll((long long)(dist - 1));
-                    in_blk = ((int64_t)c / kBlockRows) == (row / kBlockRows);
+                    in_blk = ((int64_t)c / kBlockRows) == (g / kBlockRows);
                 }
             }
             const unsigned peers = __match_any_sync(__activemask(), b);
@@ -352,11 +364,14 @@ spmm_status plan_ensure_workspace(Plan *p, size_t need) { return ensure_workspac
 //       N % 4 == 0 with 16-byte aligned operands, a ring of 3R + 2W B rows
 //       that fits in shared memory with at most 4 column tiles,
 //       an average tile's entries fitting one pipeline stage (two rows per
-//       lane group preferred, else one), and a 2W halo at most twice a CTA's
-//       row range                                              -> WINDOW;
+//       lane group preferred, else one), a 2W halo at most twice a CTA's
+//       row range, and (row-range plans) a first row on a multiple of the
+//       tile's R rows                                          -> WINDOW;
+//   R1a BLOCK (tensor cores) only when pinned;
 //   R2  wide N (more than 32 column vectors per row)        -> WARPROW with column
 //       tiles (COLTILE, the staged variant, measured 1.1-1.7x slower: pin only);
-//   R3  near-uniform degrees (CV_d <= 1) and narrow N        -> ROWGROUP, 32/L rows per warp;
+//   R3  near-uniform degrees (CV_d <= 1) and narrow N (L < 32 lanes, so
+//       several rows share a warp)                            -> ROWGROUP, 32/L rows per warp;
 //   R4  otherwise (skewed degrees)                            -> WARPROW.
 // Independently of the family, rows with more than t_split entries are split
 // into chunks (two extra launches) whenever the plan holds such rows.
@@ -387,8 +402,9 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     // 256-column diagonal blocks, block density 0.2) it measured 145 us at
     // N=128 against 94 us for WARPROW: the per-chunk staging of the operands,
     // not the tensor cores, bounds it. The router keeps it out until it wins.
+    // Its diagonal blocks are those of a plan that starts at row 0.
     if (family_override == SPMM_FAMILY_BLOCK && d->M > 0 && N > 0 && N % 16 == 0 &&
-        (aligned & 1) && reduce != SPMM_MAX)
+        (aligned & 1) && reduce != SPMM_MAX && d->row0 == 0)
         fam = SPMM_FAMILY_BLOCK;
     int64_t win_tiles = 0;
     if (window_ok && fam == -2) {
@@ -405,6 +421,8 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
                                   &w))
                     continue;
                 if (w.smem_bytes > kWindowSmemBudget) continue;
+                // a row-range plan's tiles must start on whole R-row boxes of B
+                if (d->row0 % w.R != 0) continue;
                 // the staged entries of an average tile must fit a stage (else the
                 // tile is read from global memory)
                 if (!forced && (double)w.R * d->dbar * 1.25 + 64 > (double)w.ecap) continue;
@@ -436,7 +454,9 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
             fam = family_override;
         else if (n_vec > 32)
             fam = SPMM_FAMILY_WARPROW;   // measured faster than COLTILE on the wide workloads
-        else if (d->cv <= 1.0)
+        else if (d->cv <= 1.0 && lanes < 32)
+            // a 32-lane ROWGROUP holds one row per warp like WARPROW, without
+            // WARPROW's batched loads (community graph, N=128: 104 against 94 us)
             fam = SPMM_FAMILY_ROWGROUP;
         else
             fam = SPMM_FAMILY_WARPROW;
@@ -498,12 +518,10 @@ const char *spmm_status_string(spmm_status s) {
 
 uint64_t spmm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *stream,
-                             spmm_plan_t *out) {
-    if (!out) return SPMM_ERR_INVALID_ARG;
-    *out = nullptr;
-    if (M < 0 || K < 0 || !rowptr) return SPMM_ERR_INVALID_ARG;
-    if (M >= INT32_MAX || K >= INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+// Plan over rows [row_begin, row_begin + M) of the CSR array `rowptr`. A whole
+// matrix (range == false) must have rowptr[0] == 0; a row range is rebased.
+static spmm_status create_plan(const int32_t *rowptr, int64_t row_begin, int64_t M, int64_t K,
+                               bool range, void *stream, spmm_plan_t *out) {
     const char *fault = std::getenv("SPMM_FAULT_ALLOC");
     t_alloc_countdown = fault ? std::atoi(fault) : 0;
     cudaStream_t s = (cudaStream_t)stream;
@@ -518,23 +536,33 @@ spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *
     if (e == cudaSuccess) e = dev_alloc((void **)&p->err, sizeof(int32_t) * kErrWords);
     if (e == cudaSuccess) e = cudaMemsetAsync(p->err, 0, sizeof(int32_t) * kErrWords, s);
     if (e == cudaSuccess)
-        e = cudaMemcpyAsync(p->rowptr, rowptr, sizeof(int32_t) * (M + 1), cudaMemcpyDefault, s);
+        e = cudaMemcpyAsync(p->rowptr, rowptr + row_begin, sizeof(int32_t) * (M + 1),
+                            cudaMemcpyDefault, s);
     int32_t ends[2] = {0, 0};
     if (e == cudaSuccess) e = cudaMemcpyAsync(&ends[0], p->rowptr, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaMemcpyAsync(&ends[1], p->rowptr + M, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
         st = from_cuda(e);
-    } else if (ends[0] != 0 || ends[1] < 0) {
+    } else if ((range ? ends[0] < 0 : ends[0] != 0) || ends[1] < ends[0]) {
         st = SPMM_ERR_INVALID_INPUT;
     } else if (ends[1] > INT32_MAX - 64) {
         st = SPMM_ERR_UNSUPPORTED;
     } else {
-        p->nnz = ends[1];
+        p->row0 = row_begin;
+        p->col_base = ends[0];
+        p->nnz = (int64_t)ends[1] - ends[0];
+        if (ends[0] != 0) {
+            k_rebase<<<(unsigned)std::min<int64_t>((M + 256) / 256, 4096), 256, 0, s>>>(
+                p->rowptr, M + 1, ends[0]);
+            count_launch();
+            e = cudaGetLastError();
+        }
         // pad the copy with rowptr[M] so that tile-sized bulk copies may run past row M
-        std::vector<int32_t> pad(kRowptrPad, ends[1]);
-        e = cudaMemcpyAsync(p->rowptr + M + 1, pad.data(), sizeof(int32_t) * kRowptrPad,
-                            cudaMemcpyHostToDevice, s);
+        std::vector<int32_t> pad(kRowptrPad, (int32_t)p->nnz);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(p->rowptr + M + 1, pad.data(), sizeof(int32_t) * kRowptrPad,
+                                cudaMemcpyHostToDevice, s);
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) {
             destroy(p);
@@ -550,6 +578,53 @@ spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *
         return st;
     }
     *out = reinterpret_cast<spmm_plan_t>(p);
+    return SPMM_OK;
+}
+
+spmm_status spmm_plan_create(const int32_t *rowptr, int64_t M, int64_t K, void *stream,
+                             spmm_plan_t *out) {
+    if (!out) return SPMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (M < 0 || K < 0 || !rowptr) return SPMM_ERR_INVALID_ARG;
+    if (M >= INT32_MAX || K >= INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+    return create_plan(rowptr, 0, M, K, false, stream, out);
+}
+
+spmm_status spmm_plan_create_range(const int32_t *rowptr, int64_t row_begin, int64_t row_end,
+                                   int64_t K, void *stream, spmm_plan_t *out) {
+    if (!out) return SPMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (row_begin < 0 || row_end < row_begin || K < 0 || !rowptr) return SPMM_ERR_INVALID_ARG;
+    if (row_end >= INT32_MAX || K >= INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+    return create_plan(rowptr, row_begin, row_end - row_begin, K, true, stream, out);
+}
+
+spmm_status spmm_partition_rows(const int32_t *rowptr, int64_t M, int32_t parts,
+                                int64_t align_rows, int64_t *bounds) {
+    if (!rowptr || !bounds || M < 0 || parts < 1 || align_rows < 1) return SPMM_ERR_INVALID_ARG;
+    if (M >= INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+    if (rowptr[0] != 0) return SPMM_ERR_INVALID_INPUT;
+    for (int64_t i = 0; i < M; ++i)
+        if (rowptr[i + 1] < rowptr[i]) return SPMM_ERR_INVALID_INPUT;
+    // work of the rows before row i: their entries plus one per row (its output)
+    auto work = [&](int64_t i) { return (int64_t)rowptr[i] + i; };
+    const int64_t total = work(M);
+    bounds[0] = 0;
+    for (int32_t q = 1; q < parts; ++q) {
+        const int64_t target = (int64_t)q * total / parts;   // q < 2^31, total < 2^32
+        // first row whose prefix work reaches the target
+        int64_t lo = 0, hi = M;
+        while (lo < hi) {
+            const int64_t mid = lo + (hi - lo) / 2;
+            if (work(mid) >= target) hi = mid;
+            else lo = mid + 1;
+        }
+        // nearest multiple of align_rows, kept in order and inside [0, M]
+        int64_t b = (lo + align_rows / 2) / align_rows * align_rows;
+        b = std::min(std::max(b, bounds[q - 1]), M);
+        bounds[q] = b;
+    }
+    bounds[parts] = M;
     return SPMM_OK;
 }
 
@@ -575,6 +650,7 @@ static void fill_desc(const Plan *p, spmm_plan_info *o) {
     o->rows_sorted = p->rows_sorted ? 1 : 0;
     o->blk_intra = p->blk_intra;
     o->band_cover = p->band_cover;
+    o->row0 = p->row0;
 }
 
 spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce, spmm_plan_info *out) {
@@ -607,6 +683,7 @@ spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *
     Plan *p = reinterpret_cast<Plan *>(plan);
     if (p->nnz == 0) return SPMM_OK;
     if (!col) return SPMM_ERR_INVALID_ARG;
+    col += p->col_base;
     cudaStream_t s = (cudaStream_t)stream;
     int32_t flag = 0;
     unsigned long long *d_hist = nullptr;
@@ -616,8 +693,8 @@ spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *
     if (e == cudaSuccess) e = cudaMemsetAsync(p->err + kErrBadCol, 0, sizeof(int32_t), s);
     if (e == cudaSuccess) {
         const int64_t blocks = std::min<int64_t>((p->M + 7) / 8, (int64_t)p->num_sms * 8);
-        k_check_cols<<<(unsigned)std::max<int64_t>(1, blocks), 256, 0, s>>>(p->rowptr, col, p->M,
-                                                                             p->K, p->err, d_hist);
+        k_check_cols<<<(unsigned)std::max<int64_t>(1, blocks), 256, 0, s>>>(
+            p->rowptr, col, p->M, p->K, p->row0, p->err, d_hist);
         count_launch();
         e = cudaGetLastError();
     }
@@ -680,6 +757,9 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
     if (p->nnz > 0 && (!col || !B)) return SPMM_ERR_INVALID_ARG;
     if (N >= INT32_MAX / 4) return SPMM_ERR_UNSUPPORTED;
     if (reduce != SPMM_MAX) argmax = nullptr;
+    // a row-range plan reads its rows' entries out of the full arrays
+    if (col) col += p->col_base;
+    if (val) val += p->col_base;
     const int aligned = (((uintptr_t)B % 16 == 0) && ((uintptr_t)C % 16 == 0) &&
                          ((uintptr_t)argmax % 16 == 0) ? 1 : 0) |
                         (((uintptr_t)col % 16 == 0) && ((uintptr_t)val % 16 == 0) ? 2 : 0) |
@@ -713,6 +793,7 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
     a.bias = bias;
     a.act = (int32_t)act;
     a.rows_sorted = p->rows_sorted ? 1 : 0;
+    a.row0 = p->row0;
     const bool split = p->n_heavy > 0 && r.family != SPMM_FAMILY_BLOCK;
     if (split) {
         spmm_status st = ensure_workspace(p, workspace_need(p, N, reduce));

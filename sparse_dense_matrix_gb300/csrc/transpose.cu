@@ -327,6 +327,9 @@ spmm_status spmm_transpose(spmm_plan_t plan, const int32_t *col, const float *va
     const int64_t nnz = p->nnz, K = p->K;
     if (nnz > 0 && (!col || !colT)) return SPMM_ERR_INVALID_ARG;
     if (nnz > 0 && !valT && (val || scale_mean)) return SPMM_ERR_INVALID_ARG;
+    // a row-range plan reads its rows' entries out of the full arrays
+    col += p->col_base;
+    if (val) val += p->col_base;
     cudaStream_t s = (cudaStream_t)stream;
     const int sms = p->num_sms > 0 ? p->num_sms : 1;
 

@@ -219,13 +219,16 @@ __global__ void __launch_bounds__(kWinThreads, 1)
             const int s_al = seg_b & ~3;
             const bool overflow = (seg_e - s_al) > w.ecap;
             const int e_cp = overflow ? s_al : max(s_al, min((seg_e + 3) & ~3, a.nnz4));
-            // window of the tile (empty when it lies past the last B row)
-            const int64_t win_lo = max(r0 - W, (int64_t)0);
-            const int64_t win_hi = max(min(r1 + W, a.K), win_lo);
+            // window of the tile around its global rows [g0, g1) (a row-range
+            // plan's local row 0 is global row a.row0, a multiple of R); empty
+            // when it lies past the last B row
+            const int64_t g0 = r0 + a.row0, g1 = r1 + a.row0;
+            const int64_t win_lo = max(g0 - W, (int64_t)0);
+            const int64_t win_hi = max(min(g1 + W, a.K), win_lo);
             // rows requested through this tile: whole R-row boxes when the ring
             // holds a column slice (W and the tile starts are multiples of R);
             // non-decreasing in the tile index
-            const int64_t top = w.tmap ? min(r0 + R + W, Kr) : win_hi;
+            const int64_t top = w.tmap ? min(g0 + R + W, Kr) : win_hi;
             int64_t prev = __shfl_up_sync(0xffffffffu, top, 1);
             if (lane == 0) prev = carry_hi;
             carry_hi = __shfl_sync(0xffffffffu, top, kWarp - 1);

@@ -68,6 +68,15 @@ def test_host_argument_checks(sdm):
     assert lib.spmm_route(ctypes.byref(info), 4, 7, 1, 152, -1, ctypes.byref(info)) == 1
     assert lib.spmm_route(ctypes.byref(info), -4, 0, 1, 152, -1, ctypes.byref(info)) == 1
     assert lib.spmm_route(ctypes.byref(info), 4, 0, 1, 152, 9, ctypes.byref(info)) == 1
+    assert lib.spmm_plan_create_range(None, 0, 4, 10, None, ctypes.byref(out)) == 1
+    assert out.value is None
+    assert lib.spmm_plan_create_range(ctypes.c_void_p(16), 5, 4, 10, None, ctypes.byref(out)) == 1
+    assert lib.spmm_plan_create_range(ctypes.c_void_p(16), -1, 4, 10, None, ctypes.byref(out)) == 1
+    assert lib.spmm_plan_create_range(ctypes.c_void_p(16), 0, 4, 10, None, None) == 1
+    assert lib.spmm_plan_create_range(ctypes.c_void_p(16), 0, 1 << 31, 10, None,
+                                      ctypes.byref(out)) == 5
+    b = (ctypes.c_int64 * 3)()
+    assert lib.spmm_partition_rows(None, 4, 2, 1, b) == 1
 
 
 def test_plan_create_without_a_gpu_reports_cuda_error(sdm):
@@ -105,6 +114,8 @@ def test_router_rules(sdm):
     r = sdm.spmm_route(_desc(cv=0.0), 33, 0)
     assert (r["family_name"], r["vec"], r["col_tiles"]) == ("warprow", 1, 2)
     assert sdm.spmm_route(_desc(cv=0.0), 36, 0)["family_name"] == "rowgroup"
+    r = sdm.spmm_route(_desc(cv=0.0), 128, 0)                  # 32 lanes: a warp per row
+    assert (r["family_name"], r["lanes"], r["rows_per_warp"]) == ("warprow", 32, 1)
     r = sdm.spmm_route(_desc(cv=0.0), 1, 2)
     assert (r["vec"], r["lanes"], r["rows_per_warp"]) == (1, 2, 16)
     r = sdm.spmm_route(_desc(cv=0.0), 16, 0, family=sdm.FAMILY["warprow"])
@@ -161,6 +172,13 @@ def test_router_window_rule(sdm):
     assert r["family_name"] == "window"                                           # pinned
     wide = dict(_desc(cv=0.0), band_w=4096, band_cover=0.9)
     assert sdm.spmm_route(wide, 512, 0)["family_name"] == "warprow"             # ring too big
+    # row-range plans: the tiles must start on whole R-row boxes of B
+    assert sdm.spmm_route(dict(knn, row0=1 << 19), 16, 0)["family_name"] == "window"
+    assert sdm.spmm_route(dict(knn, row0=1 << 19), 64, 0)["family_name"] == "window"
+    assert sdm.spmm_route(dict(knn, row0=1000), 16, 0)["family_name"] == "rowgroup"
+    r = sdm.spmm_route(dict(knn, row0=128), 16, 0)          # 256-row tiles do not fit: 128
+    assert (r["family_name"], r["window_rows"]) == ("window", 128)
+    assert sdm.spmm_route(dict(knn, row0=64), 16, 0)["family_name"] == "rowgroup"
 
 
 def test_router_block_rule(sdm):
@@ -179,3 +197,6 @@ def test_router_block_rule(sdm):
     assert r["family_name"] != "block"                                          # unaligned B/C
     r = sdm.spmm_route(dict(com, rows_sorted=0), 128, 0, family=pin)
     assert r["family_name"] == "block"                                          # any row order
+    r = sdm.spmm_route(dict(com, row0=256), 128, 0, family=pin)
+    assert r["family_name"] == "warprow"                                        # a row range
+
