@@ -170,10 +170,14 @@ constexpr int kSpreadBins = 34;
 constexpr int kHistWords = kSpreadBins + 2;
 // Rows are local to the plan; the spread and the diagonal blocks are measured
 // against the global row (row + row0) that a row-range plan's row stands for.
+// A warp takes one work item: a row of at most t_split entries, or one chunk
+// of a longer row from the plan's chunk table, so that no warp walks a hub
+// row of ~1e5 entries alone (that tail had set the pass's time).
 __global__ void __launch_bounds__(256) k_check_cols(const int32_t *__restrict__ rowptr,
                                                    const int32_t *__restrict__ col, int64_t M,
-                                                   int64_t K, int64_t row0,
-                                                   int32_t *__restrict__ err,
+                                                   int64_t K, int64_t row0, int64_t t_split,
+                                                   int64_t chunk, const int2 *__restrict__ chunks,
+                                                   int64_t n_chunks, int32_t *__restrict__ err,
                                                    unsigned long long *__restrict__ hist) {
     __shared__ unsigned int sh[kHistWords];
     for (int b = threadIdx.x; b < kHistWords; b += blockDim.x) sh[b] = 0;
@@ -181,10 +185,24 @@ __global__ void __launch_bounds__(256) k_check_cols(const int32_t *__restrict__ 
     int bad = 0;
     const int lane = threadIdx.x & 31;
     const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < M;
-         row += warps) {
-        const int p0 = rowptr[row], p1 = rowptr[row + 1];
-        for (int pb = p0; pb < p1; pb += 32) {
+    for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+         item < M + n_chunks; item += warps) {
+        int64_t row;
+        int p0, pa, p1;      // row start (for the order check), then the item's entries [pa, p1)
+        if (item < M) {
+            row = item;
+            p0 = rowptr[row];
+            p1 = rowptr[row + 1];
+            if (p1 - p0 > t_split) continue;            // uniform per warp: chunked below
+            pa = p0;
+        } else {
+            const int2 ch = chunks[item - M];
+            row = ch.x;
+            pa = ch.y;
+            p0 = rowptr[row];
+            p1 = (int)min((int64_t)pa + chunk, (int64_t)rowptr[row + 1]);
+        }
+        for (int pb = pa; pb < p1; pb += 32) {
             const int p = pb + lane;
             int b = -1;
             bool in_blk = false, descent = false;
@@ -694,7 +712,8 @@ spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *
     if (e == cudaSuccess) {
         const int64_t blocks = std::min<int64_t>((p->M + 7) / 8, (int64_t)p->num_sms * 8);
         k_check_cols<<<(unsigned)std::max<int64_t>(1, blocks), 256, 0, s>>>(
-            p->rowptr, col, p->M, p->K, p->row0, p->err, d_hist);
+            p->rowptr, col, p->M, p->K, p->row0, p->t_split, p->chunk, p->chunks, p->n_chunks,
+            p->err, d_hist);
         count_launch();
         e = cudaGetLastError();
     }
