@@ -87,6 +87,8 @@ def parse():
                     help="comma-separated feature widths to run (default: all of the workload's)")
     ap.add_argument("--reduce", default=None,
                     help="comma-separated reductions to run (default: all of the workload's)")
+    ap.add_argument("--graph-batch", type=int, default=50,
+                    help="launches per CUDA graph for the graph-batched figure (0: skip)")
     ap.add_argument("--warm-iters", type=int, default=20,
                     help="back-to-back launches per run for the warm-L2 figure (0: skip)")
     return ap.parse_args()
@@ -342,10 +344,10 @@ def run_ours(args):
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def one(n, r):
+    def one(n, r, on=None):
         sdm.spmm_run(adj.plan, col.data_ptr(), None if val is None else val.data_ptr(),
                      Bd[n].data_ptr(), n, sdm.REDUCE[r], Cd[n].data_ptr(),
-                     Ad[n].data_ptr() if r == "max" else None, stream)
+                     Ad[n].data_ptr() if r == "max" else None, stream if on is None else on)
 
     def flush_l2():
         # overwrite L2, then hold the stream ~50 us so that the host has enqueued
@@ -399,6 +401,37 @@ def run_ours(args):
         warm_ms = [float(np.median([a.elapsed_time(b) for a, b in wev[k]]))
                    for k in range(len(runs))]
 
+    # CUDA-graph figure, also outside the timed region and not part of value:
+    # G launches of each run captured back to back in one graph and replayed,
+    # so a small problem is timed without the per-launch CPU and launch gaps
+    # (warm L2). For a workload of well under a megabyte (the 2k-row graph)
+    # this is the figure that the launch overhead otherwise hides.
+    graph_ms = [None] * len(runs)
+    graph_note = None
+    if args.graph_batch > 0:
+        try:
+            gs = torch.cuda.Stream(dev)
+            gs.wait_stream(stream)
+            for k, (n, r) in enumerate(runs):
+                cg = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(cg, stream=gs, capture_error_mode="relaxed"):
+                    for _ in range(args.graph_batch):
+                        one(n, r, gs)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(gs):
+                    cg.replay()
+                    e0.record(gs)
+                    cg.replay()
+                    e1.record(gs)
+                torch.cuda.synchronize()
+                graph_ms[k] = e0.elapsed_time(e1) / args.graph_batch
+                del cg
+        except Exception as exc:     # capture unsupported here: report why, keep the line
+            graph_ms = [None] * len(runs)
+            graph_note = f"not measured: {type(exc).__name__}: {exc}"[:200]
+        torch.cuda.synchronize()
+
     per_run_ms = np.array([[a.elapsed_time(b) for a, b in ev[s]] for s in range(args.steps)])
     dev_ms = float(per_run_ms.sum())
     if pg is not None:
@@ -430,6 +463,7 @@ def run_ours(args):
                         "ms_p10": float(np.percentile(per_run_ms[:, k], 10)),
                         "ms_p90": float(np.percentile(per_run_ms[:, k], 90)),
                         "warm_l2_ms": warm_ms[k],
+                        "graph_batched_ms": graph_ms[k],
                         "gflops": 2.0 * g.nnz * n / (np.median(per_run_ms[:, k]) / 1e3) / 1e9,
                         "hbm_frac": b / (np.median(per_run_ms[:, k]) / 1e3) / 1e9 / hbm_peak})
 
@@ -520,6 +554,10 @@ def run_ours(args):
                                  "per_run ms is the median over steps, with p10 and p90",
                        "warm_l2": "per_run warm_l2_ms: back-to-back launches without the "
                                   "flush, after the timed region; not part of value",
+                       "graph_batched": graph_note or (
+                           f"per_run graph_batched_ms: per-launch time of {args.graph_batch} "
+                           "launches captured in one CUDA graph (warm L2, no launch gaps), "
+                           "after the timed region; not part of value"),
                        "per_run": per_run},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clk, "cold_path": cold,
