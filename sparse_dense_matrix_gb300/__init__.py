@@ -385,7 +385,9 @@ class SparseAdj:
     def transpose(self, scale_mean: bool = False) -> "SparseAdj":
         """A^T as a new SparseAdj (K x M). With ``scale_mean`` the value of entry
         (i, j) is a_ij / d_i, so that ``adj.transpose(True) @ dC`` is the
-        gradient of ``adj.reduce(B, "mean")`` with respect to B."""
+        gradient of ``adj.reduce(B, "mean")`` with respect to B. For a row range
+        (``rows=(b, e)``) the result is K x (e - b), its columns the range's
+        local row numbers."""
         import torch
         nnz = self.nnz
         rowptrT = torch.empty(self.K + 1, dtype=torch.int32, device=self.device)
