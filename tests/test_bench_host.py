@@ -1,0 +1,30 @@
+"""Host-side pieces of bench.py that need no GPU: run selection and the
+roofline numerator (compulsory bytes) on the 2k-row Erdos-Renyi workload."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def test_run_selection():
+    import bench
+    spec, g, runs = bench.workload(1)
+    assert runs == [(32, "sum"), (32, "mean"), (32, "max")] and g.M == g.K == 2048
+    spec, g, runs = bench.workload(1, "32", "max")
+    assert runs == [(32, "max")] and list(spec["N"]) == [32] and list(spec["reduce"]) == ["max"]
+    with pytest.raises(SystemExit):
+        bench.workload(1, "7", None)           # not one of the workload's widths
+    with pytest.raises(SystemExit):
+        bench.workload(1, None, "min")
+
+
+def test_compulsory_bytes_by_hand():
+    import bench
+    _, g, _ = bench.workload(1)
+    assert g.nnz == 16384 and g.val is not None
+    # rowptr 4 * 2049, col + val 8 * 16384, B 4 * 2048 * 32, C 4 * 2048 * 32
+    assert bench.compulsory_bytes(g, 32, "sum") == 8196 + 131072 + 262144 + 262144
+    assert bench.compulsory_bytes(g, 32, "max") == 8196 + 131072 + 3 * 262144   # + argmax
