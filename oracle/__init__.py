@@ -20,7 +20,8 @@ tolerance |err| <= 1e-5 * T + 1e-6.
 Backward (graph-spmm card, "Requirements and limits" and "API"): ``transpose``
 builds A^T in CSR (stable by row; optionally each value divided by its row's
 degree, for the mean), so that the sum / mean backward is a product with it;
-``maxpool_backward`` routes dC[i, k] to the forward argmax column.
+``maxpool_backward`` routes dC[i, k] to the forward argmax column, through the
+one stored entry (of a duplicated pair) whose product won.
 """
 from __future__ import annotations
 
@@ -84,7 +85,7 @@ class Oracle:
         lib.oracle_threads.restype = ctypes.c_int
         lib.oracle_transpose.argtypes = [i64, i64, p, p, p, ctypes.c_int, p, p, p]
         lib.oracle_transpose.restype = ctypes.c_int
-        lib.oracle_maxpool_backward.argtypes = [i64, i64, i64, p, p, p, p, p, p]
+        lib.oracle_maxpool_backward.argtypes = [i64, i64, i64, p, p, p, p, p, p, p]
         lib.oracle_maxpool_backward.restype = ctypes.c_int
         self.lib = lib
 
@@ -144,16 +145,21 @@ class Oracle:
             raise ValueError("oracle_transpose rejected its arguments")
         return rT, cT, vT
 
-    def maxpool_backward(self, rowptr, col, val, argmax, dC, K):
-        """dB [K, N] of the max reduction, given the forward argmax and dC [M, N]."""
+    def maxpool_backward(self, rowptr, col, val, argmax, dC, K, B=None):
+        """dB [K, N] of the max reduction, given the forward argmax, dC [M, N]
+        and, for a weighted A, the forward's B [K, N] (it decides which stored
+        copy of a duplicated pair won)."""
         rowptr = np.ascontiguousarray(rowptr, dtype=np.int32)
         col = np.ascontiguousarray(col, dtype=np.int32)
         val = None if val is None else np.ascontiguousarray(val, dtype=np.float32)
         argmax = np.ascontiguousarray(argmax, dtype=np.int32)
         dC = np.ascontiguousarray(dC, dtype=np.float32)
+        B = None if B is None else np.ascontiguousarray(B, dtype=np.float32)
         M, N = dC.shape
+        if B is not None and B.shape != (K, N):
+            raise ValueError("B must be [K, N]")
         dB = np.empty((K, N), np.float32)
-        if self.lib.oracle_maxpool_backward(M, K, N, _ptr(rowptr), _ptr(col), _ptr(val),
+        if self.lib.oracle_maxpool_backward(M, K, N, _ptr(rowptr), _ptr(col), _ptr(val), _ptr(B),
                                             _ptr(argmax), _ptr(dC), _ptr(dB)) != 0:
             raise ValueError("oracle_maxpool_backward rejected its arguments")
         return dB
@@ -197,6 +203,8 @@ def transpose(rowptr, col, val, K, scale_mean=False):
     return _default().transpose(rowptr, col, val, K, scale_mean)
 
 
-def maxpool_backward(rowptr, col, val, argmax, dC, K):
-    """Gradient of the max reduction with respect to B."""
-    return _default().maxpool_backward(rowptr, col, val, argmax, dC, K)
+def maxpool_backward(rowptr, col, val, argmax, dC, K, B=None):
+    """Gradient of the max reduction with respect to B: dC[i, k] times the
+    weight of the stored entry that won the forward maximum (B is needed when
+    A is weighted)."""
+    return _default().maxpool_backward(rowptr, col, val, argmax, dC, K, B)

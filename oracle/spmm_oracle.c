@@ -267,9 +267,15 @@ int oracle_descriptors(int64_t M, const int32_t *rowptr, oracle_desc *out) {
  * of entry (i, j) is a_ij / d_i rounded once (1 / d_i for an unweighted A):
  * then A_mean^T . dC is the mean's backward.
  *
- * oracle_maxpool_backward: dB[j, k] = sum over rows i with argmax[i, k] == j
- * and over the stored entries p of row i with col[p] == j of a_p * dC[i, k]
- * (fp64, rounded once). A duplicated winning pair contributes once per copy.
+ * oracle_maxpool_backward: the derivative of the max reduction with respect
+ * to B. The forward value C[i, k] is the product y_p = fl32(a_p * B[j_p, k])
+ * of ONE stored entry p of row i (duplicates are legal CSR, graph-spmm card,
+ * "Correctness"), so only that entry passes the gradient:
+ *   dB[j, k] = sum over rows i with argmax[i, k] == j of a_w * dC[i, k],
+ * where w is the winning copy of column j in row i: among the stored entries p
+ * of row i with col[p] == j, the one with the largest y_p, the smallest
+ * storage position on equal y_p (fp64 sum, rounded once). Without duplicated
+ * pairs w is the only entry of column j in the row.
  * ------------------------------------------------------------------------ */
 int oracle_transpose(int64_t M, int64_t K, const int32_t *rowptr, const int32_t *col,
                      const float *val, int scale_mean, int32_t *rowptrT, int32_t *colT,
@@ -301,17 +307,29 @@ int oracle_transpose(int64_t M, int64_t K, const int32_t *rowptr, const int32_t 
 }
 
 int oracle_maxpool_backward(int64_t M, int64_t K, int64_t N, const int32_t *rowptr,
-                            const int32_t *col, const float *val, const int32_t *argmax,
-                            const float *dC, float *dB) {
+                            const int32_t *col, const float *val, const float *B,
+                            const int32_t *argmax, const float *dC, float *dB) {
     if (M < 0 || K < 0 || N < 0 || !rowptr || !argmax || !dC || !dB) return -1;
+    if (val && !B && rowptr[M] > 0) return -1;
     double *acc = (double *)calloc((size_t)(K * N > 0 ? K * N : 1), sizeof(double));
     if (!acc) return -1;
     for (int64_t i = 0; i < M; ++i) {
-        for (int64_t p = rowptr[i]; p < rowptr[i + 1]; ++p) {
-            const int32_t j = col[p];
-            const double a = val ? (double)val[p] : 1.0;
-            for (int64_t k = 0; k < N; ++k)
-                if (argmax[i * N + k] == j) acc[(int64_t)j * N + k] += a * (double)dC[i * N + k];
+        for (int64_t k = 0; k < N; ++k) {
+            const int32_t j = argmax[i * N + k];
+            if (j < 0) continue;                      /* empty row: no gradient */
+            if (j >= K) { free(acc); return -1; }
+            /* the winning copy of column j: largest fp32 product, first on ties */
+            int64_t w = -1;
+            float y_w = 0.0f;
+            for (int64_t p = rowptr[i]; p < rowptr[i + 1]; ++p) {
+                if (col[p] != j) continue;
+                const float a = val ? val[p] : 1.0f;
+                const float y = val ? (float)((double)a * (double)B[(int64_t)j * N + k]) : 0.0f;
+                if (w < 0 || y > y_w) { w = p; y_w = y; }
+            }
+            if (w < 0) { free(acc); return -1; }      /* argmax names no stored column */
+            const double a_w = val ? (double)val[w] : 1.0;
+            acc[(int64_t)j * N + k] += a_w * (double)dC[i * N + k];
         }
     }
     for (int64_t q = 0; q < K * N; ++q) dB[q] = (float)acc[q];
