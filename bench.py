@@ -7,8 +7,13 @@ plan (descriptors, heavy-row tables, workspace) is built before timing, as a
 GNN layer reuses it. Device time comes from CUDA events around each run on
 the launching stream; value = sum of 2*nnz*N over the timed runs / that time.
 
-Default workload: kNN/road-like locality graph, M = K = 1,048,576, 10 distinct
-neighbours within +-512 of the row id, unweighted, N in {16, 64}, sum and mean.
+Default workload: the largest configuration, a Chung-Lu power-law graph with
+M = K = 4,194,304 (degree exponent 2.1, mean 25, capped at 100,000; ids
+randomly permuted; about 105M weighted entries), N in {16, 64, 256}, sum,
+mean and max + argmax. ``--n`` selects other widths of its sweep
+{16, 32, 64, 128, 256}. Beside it the line carries ``per_config``: the sum
+runs of the four other workloads (Erdos-Renyi 2k, kNN 1M, R-MAT scale 20,
+community 64k), each timed the same way.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
 
@@ -34,48 +39,64 @@ sys.path.insert(0, ROOT)
 
 METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
 
-# DRAM bytes per launch of the dominant kernel from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel and the
-# workload; None until a capture of the current kernel exists.
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# `ncu --set full` capture of the bench step (profiles/window_knn1M_bench.md). The
-# counters belong to the kernel build they were taken on: "sources_sha256" is the
-# sha256 of the WINDOW kernel's sources then (kernel_sources_sha256()), and the
-# bench reports traffic as null once they differ.
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
+# family's kernels on a workload run, from one ncu capture. The counters belong
+# to the kernel build they were taken on: "sources_sha256" is the sha256 of the
+# family's sources then (family_sources_sha256()), and the bench reports the
+# traffic as null once they differ.
 NCU_TRAFFIC = {
-    "sources_sha256": "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af",
-    "window/knn_1M/N16/sum": 149.09e6,
-    "window/knn_1M/N16/mean": 148.67e6,
-    "window/knn_1M/N64/sum": 557.30e6,
-    "window/knn_1M/N64/mean": 559.95e6,
+    "window/knn_1M/N16/sum": {"bytes": 149.09e6, "sources_sha256":
+                              "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af"},
+    "window/knn_1M/N16/mean": {"bytes": 148.67e6, "sources_sha256":
+                               "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af"},
+    "window/knn_1M/N64/sum": {"bytes": 557.30e6, "sources_sha256":
+                              "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af"},
+    "window/knn_1M/N64/mean": {"bytes": 559.95e6, "sources_sha256":
+                               "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af"},
+}
+
+_CSRC = "sparse_dense_matrix_gb300/csrc/"
+# the sources each family's kernels are built from
+FAMILY_SOURCES = {
+    "window": (_CSRC + "common.cuh", _CSRC + "tma.cuh", _CSRC + "window.cuh",
+               _CSRC + "f_window.cu", _CSRC + "f_window_sum.cu", _CSRC + "f_window_mean.cu",
+               _CSRC + "f_window_max.cu", "include/spmm.h"),
+    "warprow": (_CSRC + "common.cuh", _CSRC + "f_warprow.cu", _CSRC + "plan.cu",
+                "include/spmm.h"),
 }
 
 
-# the sources the WINDOW kernel (the bench's dominant kernel) is built from
-WINDOW_SOURCES = ("sparse_dense_matrix_gb300/csrc/common.cuh", "sparse_dense_matrix_gb300/csrc/tma.cuh",
-                  "sparse_dense_matrix_gb300/csrc/window.cuh", "sparse_dense_matrix_gb300/csrc/f_window.cu",
-                  "sparse_dense_matrix_gb300/csrc/f_window_sum.cu",
-                  "sparse_dense_matrix_gb300/csrc/f_window_mean.cu",
-                  "sparse_dense_matrix_gb300/csrc/f_window_max.cu", "include/spmm.h")
-
-
-def kernel_sources_sha256():
+def family_sources_sha256(family):
     h = hashlib.sha256()
-    for rel in WINDOW_SOURCES:
+    for rel in FAMILY_SOURCES.get(family, ()):
         h.update(rel.encode())
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
+
+def ncu_traffic(key, family):
+    """ncu DRAM bytes per launch for a run key, or None (no capture, or the
+    family's sources changed since)."""
+    ent = NCU_TRAFFIC.get(key)
+    if ent is None or family not in FAMILY_SOURCES:
+        return None
+    return ent["bytes"] if family_sources_sha256(family) == ent["sources_sha256"] else None
+
+
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0    # the ~8 TB/s GB300 HBM3e figure the 60% target is stated against
+# widths timed by default where the workload's sweep is longer: its two ends
+# and the middle
+DEFAULT_N = {5: (16, 64, 256)}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--family", default="auto",
                     choices=["auto", "rowgroup", "warprow", "coltile", "window", "block"])
@@ -91,6 +112,9 @@ def parse():
                     help="launches per CUDA graph for the graph-batched figure (0: skip)")
     ap.add_argument("--warm-iters", type=int, default=20,
                     help="back-to-back launches per run for the warm-L2 figure (0: skip)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the sum runs of the other workloads")
+    ap.add_argument("--per-config-reps", type=int, default=20)
     return ap.parse_args()
 
 
@@ -132,7 +156,7 @@ def workload(cid, n_sel=None, r_sel=None):
     step; n_sel / r_sel restrict the runs to a comma-separated subset."""
     import gen
     spec = gen.CONFIGS[cid]
-    Ns = spec["N"] if n_sel is None else [int(x) for x in n_sel.split(",")]
+    Ns = DEFAULT_N.get(cid, spec["N"]) if n_sel is None else [int(x) for x in n_sel.split(",")]
     Rs = spec["reduce"] if r_sel is None else r_sel.split(",")
     bad = [n for n in Ns if n not in spec["N"]] + [r for r in Rs if r not in spec["reduce"]]
     if bad:
@@ -298,6 +322,49 @@ def run_reference(args):
     print(json.dumps(out))
 
 
+def other_configs(sdm, dev, cids, reps, flush_l2, stream, hbm_peak):
+    """The sum runs of other workloads, timed like the bench's own runs (L2
+    flushed before each launch, CUDA events, median of `reps`)."""
+    import torch
+    import gen
+    out = []
+    for cid in cids:
+        spec = gen.CONFIGS[cid]
+        if "sum" not in spec["reduce"]:
+            continue
+        g = gen.config(cid)
+        rp = torch.from_numpy(g.rowptr).to(dev)
+        cl = torch.from_numpy(g.col).to(dev)
+        vl = None if g.val is None else torch.from_numpy(g.val).to(dev)
+        adj = sdm.SparseAdj(rp, cl, vl, num_cols=g.K)
+        for n in spec["N"]:
+            Bd = torch.from_numpy(gen.features(g.K, n, seed=0)).to(dev)
+            Cd = torch.empty((g.M, n), dtype=torch.float32, device=dev)
+            adj.reserve(n, "sum")
+            for _ in range(3):
+                adj.reduce(Bd, "sum", out=Cd, stream=stream)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for a, b in evs:
+                flush_l2()
+                a.record(stream)
+                adj.reduce(Bd, "sum", out=Cd, stream=stream)
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = float(np.median([a.elapsed_time(b) for a, b in evs]))
+            by = compulsory_bytes(g, n, "sum")
+            out.append({"workload": spec["name"], "N": n, "reduce": "sum",
+                        "family": adj.describe(n, "sum")["family_name"], "ms": ms,
+                        "gflops": 2.0 * g.nnz * n / (ms / 1e3) / 1e9,
+                        "hbm_frac": by / (ms / 1e3) / 1e9 / hbm_peak,
+                        "hbm_frac_nominal": by / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS})
+            del Bd, Cd
+        adj.close()
+        del rp, cl, vl
+    torch.cuda.synchronize()
+    return out
+
+
 def run_ours(args):
     import torch
     world, rank, local, pg = dist_init(args)
@@ -381,8 +448,23 @@ def run_ours(args):
         pg.barrier()
     t1 = time.time()
     launches = sdm.spmm_launch_count() - launches0
+    # nvidia-smi samples every 100 ms: when the timed steps took less than a
+    # second, the same steps run on (untimed, same work) with the sampler still
+    # going until one second has passed, so that the clock record covers them
+    t_clk = t1
+    extra = 0
+    while t_clk - t0 < 1.0:
+        for n, r in runs:
+            flush_l2()
+            one(n, r)
+        torch.cuda.synchronize()
+        extra += 1
+        t_clk = time.time()
     sdm.spmm_plan_sync(adj.plan)
-    clk = clocks.stop(t0, t1)
+    clk = clocks.stop(t0, t_clk)
+    clk["region_s"] = t_clk - t0
+    clk["region"] = (f"the {args.steps} timed steps" +
+                     (f" and {extra} more untimed steps of the same work" if extra else ""))
 
     # Warm-L2 figure, outside the timed region and not part of value: each run
     # launched back to back without the flush, so B, col and C stay in L2 as far
@@ -407,15 +489,19 @@ def run_ours(args):
     # (warm L2). For a workload of well under a megabyte (the 2k-row graph)
     # this is the figure that the launch overhead otherwise hides.
     graph_ms = [None] * len(runs)
+    graph_nb = [None] * len(runs)
     graph_note = None
+    mean_run_ms = np.array([[a.elapsed_time(b) for a, b in ev[s_]] for s_ in range(args.steps)]).mean(axis=0)
     if args.graph_batch > 0:
         try:
             gs = torch.cuda.Stream(dev)
             gs.wait_stream(stream)
             for k, (n, r) in enumerate(runs):
+                # about 5 ms of launches per graph (at most --graph-batch)
+                nb = int(max(1, min(args.graph_batch, round(5.0 / max(mean_run_ms[k], 1e-3)))))
                 cg = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(cg, stream=gs, capture_error_mode="relaxed"):
-                    for _ in range(args.graph_batch):
+                    for _ in range(nb):
                         one(n, r, gs)
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
@@ -425,7 +511,8 @@ def run_ours(args):
                     cg.replay()
                     e1.record(gs)
                 torch.cuda.synchronize()
-                graph_ms[k] = e0.elapsed_time(e1) / args.graph_batch
+                graph_ms[k] = e0.elapsed_time(e1) / nb
+                graph_nb[k] = nb
                 del cg
         except Exception as exc:     # capture unsupported here: report why, keep the line
             graph_ms = [None] * len(runs)
@@ -440,18 +527,18 @@ def run_ours(args):
     value = flops_step * args.steps * world / (dev_ms / 1e3) / 1e9
 
     hbm_peak, peak_kind = peaks()
-    # dominant kernel: the run with the largest mean device time
-    mean_ms = per_run_ms.mean(axis=0)
-    kdom = int(np.argmax(mean_ms))
+    # dominant kernel: the run with the largest median device time
+    med_ms = np.median(per_run_ms, axis=0)
+    kdom = int(np.argmax(med_ms))
     n_dom, r_dom = runs[kdom]
     info = adj.describe(n_dom, r_dom)
     bytes_dom = compulsory_bytes(g, n_dom, r_dom)
-    achieved = bytes_dom / (mean_ms[kdom] / 1e3) / 1e9
+    achieved = bytes_dom / (med_ms[kdom] / 1e3) / 1e9
     key = f"{info['family_name']}/{spec['name']}/N{n_dom}/{r_dom}"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak,
-                "traffic": (NCU_TRAFFIC.get(key) if kernel_sources_sha256() ==
-                            NCU_TRAFFIC["sources_sha256"] else None),
+                "frac": achieved / hbm_peak, "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                "nominal_peak": NOMINAL_HBM_GBS, "duration": "median of the run's steps",
+                "traffic": ncu_traffic(key, info["family_name"]),
                 "kernel": key, "peak_source": peak_kind,
                 "algorithmic_bytes_per_launch": bytes_dom,
                 "launches_per_run": info["launches"]}
@@ -464,8 +551,11 @@ def run_ours(args):
                         "ms_p90": float(np.percentile(per_run_ms[:, k], 90)),
                         "warm_l2_ms": warm_ms[k],
                         "graph_batched_ms": graph_ms[k],
+                        "graph_launches": graph_nb[k],
                         "gflops": 2.0 * g.nnz * n / (np.median(per_run_ms[:, k]) / 1e3) / 1e9,
-                        "hbm_frac": b / (np.median(per_run_ms[:, k]) / 1e3) / 1e9 / hbm_peak})
+                        "hbm_frac": b / (np.median(per_run_ms[:, k]) / 1e3) / 1e9 / hbm_peak,
+                        "hbm_frac_nominal": b / (np.median(per_run_ms[:, k]) / 1e3) / 1e9
+                        / NOMINAL_HBM_GBS})
 
     # End to end through the public API with pinned host buffers: every step
     # copies each feature matrix in once (one per N) and every result out; the
@@ -537,6 +627,53 @@ def run_ours(args):
                "timing": "wall clock, synchronised on both sides; two buffer sets, so copies "
                          "in, kernels and copies out of consecutive steps overlap"}
 
+    # Reuse break-even: the plan-free entry point (spmm_run_noalloc, which
+    # finds the split rows on every call) against the planned call; the plan
+    # and its column check pay for themselves after break_even_calls calls.
+    try:
+        Cn = torch.empty_like(Cd[n1])
+        An = torch.empty_like(Ad[n1]) if r1 == "max" else None
+
+        def noalloc():
+            sdm.spmm_run_noalloc(rowptr.data_ptr(), col.data_ptr(),
+                                 None if val is None else val.data_ptr(), Bd[n1].data_ptr(),
+                                 g.M, g.K, n1, sdm.REDUCE[r1], Cn.data_ptr(),
+                                 None if An is None else An.data_ptr(), stream)
+        noalloc()
+        ts_ = []
+        for _ in range(5):
+            flush_l2()
+            torch.cuda.synchronize()
+            t_a = time.perf_counter()
+            noalloc()
+            torch.cuda.synchronize()
+            ts_.append((time.perf_counter() - t_a) * 1e3)
+        ts_p = []
+        for _ in range(5):
+            flush_l2()
+            torch.cuda.synchronize()
+            t_a = time.perf_counter()
+            one(n1, r1)
+            torch.cuda.synchronize()
+            ts_p.append((time.perf_counter() - t_a) * 1e3)
+        na_ms, pl_ms = float(np.median(ts_)), float(np.median(ts_p))
+        gain = na_ms - pl_ms
+        plan_cost = cold["plan_create_ms"] + cold["validate_cols_ms"]
+        cold.update({"noalloc_call_ms": na_ms, "planned_call_ms": pl_ms,
+                     "break_even_calls": (plan_cost / gain) if gain > 0 else None,
+                     "break_even": f"(plan_create_ms + validate_cols_ms) / (noalloc_call_ms - "
+                                   f"planned_call_ms) for N={n1} {r1}, both calls wall clock "
+                                   "after an L2 flush; null when the plan-free call is not "
+                                   "slower"})
+        del Cn, An
+    except Exception as exc:
+        cold["break_even"] = f"not measured: {type(exc).__name__}: {exc}"[:200]
+
+    per_config = None
+    if not args.no_per_config:
+        per_config = other_configs(sdm, dev, [c for c in (1, 2, 3, 4) if c != args.config],
+                                   args.per_config_reps, flush_l2, stream, hbm_peak)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v, t, desc, cores = cpu_leg(g, B_host, runs, budget_s=15.0)
@@ -555,11 +692,15 @@ def run_ours(args):
                        "warm_l2": "per_run warm_l2_ms: back-to-back launches without the "
                                   "flush, after the timed region; not part of value",
                        "graph_batched": graph_note or (
-                           f"per_run graph_batched_ms: per-launch time of {args.graph_batch} "
-                           "launches captured in one CUDA graph (warm L2, no launch gaps), "
-                           "after the timed region; not part of value"),
-                       "per_run": per_run},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                           "per_run graph_batched_ms: per-launch time of graph_launches "
+                           "launches (about 5 ms of work, at most "
+                           f"{args.graph_batch}) captured in one CUDA graph (warm L2, no "
+                           "launch gaps), after the timed region; not part of value"),
+                       "per_run": per_run,
+                       "per_config": "per_config: the sum runs of the other workloads, each "
+                                     "timed as the runs above (median of "
+                                     f"{args.per_config_reps}); not part of value"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "per_config": per_config,
             "gpu_launches": int(launches), "clocks": clk, "cold_path": cold,
             "hbm_gbs_compulsory": sum(compulsory_bytes(g, n, r) for n, r in runs) * args.steps
             / (dev_ms / 1e3) / 1e9,

@@ -255,6 +255,7 @@ spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce,
 /*
  * spmm_plan_set_family -- pin the light-row family (SPMM_FAMILY_AUTO restores
  * the router) and the heavy-row threshold (t_split <= 0 restores the default;
+ * a threshold above INT32_MAX is taken as INT32_MAX, i.e. no row is split;
  * a new threshold rebuilds the heavy-row tables, synchronously on the legacy
  * default stream). For tests and benchmarks of individual families.
  */
@@ -340,27 +341,36 @@ spmm_status spmm_transpose(spmm_plan_t plan, const int32_t *col, const float *va
 /*
  * spmm_maxpool_backward -- the gradient of spmm_max with respect to B
  * (graph-spmm model card, "API": spmm_max returns the argmax so that the
- * max-pool backward can route the gradient to the winning column).
+ * max-pool backward can route the gradient to the winning column;
+ * "Correctness": duplicated pairs are legal CSR).
  *   planT  : the plan of A^T (K x M), built from spmm_transpose's rowptrT.
  *   colT, valT : spmm_transpose's output (valT unscaled, or NULL when A is
  *            unweighted).
+ *   B      : device, fp32 [K, N], the forward's B. Required when valT is not
+ *            NULL (it decides which copy of a duplicated pair won); may be
+ *            NULL for an unweighted A.
  *   argmax : device, int32 [M, N], as written by spmm_run with SPMM_MAX.
  *   dC     : device, fp32 [M, N], the gradient of C.
  *   dB     : device, fp32 [K, N], written once per element:
- *            dB[j, c] = sum over the entries (i, j) of A with argmax[i, c] == j
- *            of a_ij * dC[i, c] (every stored copy of a duplicated pair counts),
- *            accumulated in fp32 in increasing i; 0 where no row chose j. Rows
- *            of A^T longer than planT's split threshold (hub columns of A) are
- *            cut into planT's chunks: each chunk is summed in increasing i,
- *            then the chunks in order (no atomics; reproducible).
+ *            dB[j, c] = sum over the rows i with argmax[i, c] == j of
+ *            a_w * dC[i, c], where w is the stored entry of row i whose
+ *            product won the forward maximum: among the copies of (i, j), the
+ *            one with the largest fp32 product a * B[j, c], the first in CSR
+ *            order on equal products (so an unweighted duplicated pair passes
+ *            dC once). Accumulated in fp32 in increasing i; 0 where no row
+ *            chose j. Rows of A^T longer than planT's split threshold (hub
+ *            columns of A) are cut into planT's chunks: each chunk is summed
+ *            in increasing i, then the chunks in order (no atomics;
+ *            reproducible).
  * Asynchronous, except that the first call with split rows at a given N
  * grows planT's workspace with cudaMalloc (spmm_plan_reserve(planT, N,
  * SPMM_SUM) beforehand keeps allocation out). 128-bit loads when N % 4 == 0
- * and argmax, dC and dB are 16-byte aligned.
+ * and B, argmax, dC and dB are 16-byte aligned. SPMM_ERR_INVALID_ARG when a
+ * required pointer is NULL.
  */
 spmm_status spmm_maxpool_backward(spmm_plan_t planT, const int32_t *colT, const float *valT,
-                                  const int32_t *argmax, const float *dC, int64_t N, float *dB,
-                                  void *stream);
+                                  const float *B, const int32_t *argmax, const float *dC,
+                                  int64_t N, float *dB, void *stream);
 
 /*
  * spmm_check_wait_timeout -- diagnostic of the failure path. Every spin-wait in

@@ -100,7 +100,7 @@ def _load():
         "spmm_run_noalloc": ([vp, vp, vp, vp, i64, i64, i64, i32, vp, vp, vp], i32),
         "spmm_transpose": ([vp, vp, vp, i32, vp, vp, vp, vp], i32),
         "spmm_check_wait_timeout": ([vp, i64, vp], i32),
-        "spmm_maxpool_backward": ([vp, vp, vp, vp, vp, i64, vp, vp], i32),
+        "spmm_maxpool_backward": ([vp, vp, vp, vp, vp, vp, i64, vp, vp], i32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(L, name)
@@ -249,11 +249,12 @@ def spmm_check_wait_timeout(plan: int, limit_us: int, stream=None) -> int:
     return int(lib.spmm_check_wait_timeout(plan, limit_us, _stream_handle(stream)))
 
 
-def spmm_maxpool_backward(planT: int, colT_ptr, valT_ptr, argmax_ptr, dC_ptr, N: int, dB_ptr: int,
-                          stream=None) -> None:
-    """Gradient of spmm_max with respect to B, through the plan of A^T."""
-    _check(lib.spmm_maxpool_backward(planT, colT_ptr, valT_ptr, argmax_ptr, dC_ptr, N, dB_ptr,
-                                     _stream_handle(stream)), "spmm_maxpool_backward")
+def spmm_maxpool_backward(planT: int, colT_ptr, valT_ptr, B_ptr, argmax_ptr, dC_ptr, N: int,
+                          dB_ptr: int, stream=None) -> None:
+    """Gradient of spmm_max with respect to B, through the plan of A^T (B_ptr:
+    the forward's B, required for a weighted A)."""
+    _check(lib.spmm_maxpool_backward(planT, colT_ptr, valT_ptr, B_ptr, argmax_ptr, dC_ptr, N,
+                                     dB_ptr, _stream_handle(stream)), "spmm_maxpool_backward")
 
 
 # ------------------------------------------------------------ tensor API
@@ -401,15 +402,23 @@ class SparseAdj:
                            None if valT is None else valT.data_ptr())
         return SparseAdj(rowptrT, colT, valT, num_cols=self.M)
 
-    def maxpool_backward(self, argmax, grad, out=None, stream=None):
+    def maxpool_backward(self, argmax, grad, B=None, out=None, stream=None):
         """Called on A^T (from ``transpose()``): the gradient of the max
-        reduction with respect to B, given its argmax [M, N] and dC [M, N]."""
+        reduction with respect to B, given its argmax [M, N], dC [M, N] and,
+        for a weighted A, the forward's B [K, N] (which copy of a duplicated
+        pair won depends on it)."""
         import torch
         _req(argmax, torch.int32, "argmax", self.device)
         _req(grad, torch.float32, "grad", self.device)
         if grad.dim() != 2 or grad.shape[0] != self.K or tuple(argmax.shape) != tuple(grad.shape):
             raise ValueError("argmax and grad must both be [M, N] with M the rows of A")
         N = grad.shape[1]
+        if B is not None:
+            _req(B, torch.float32, "B", self.device)
+            if tuple(B.shape) != (self.M, N):
+                raise ValueError("B must be [K, N] with K the columns of A")
+        elif self.val is not None:
+            raise ValueError("a weighted A needs the forward's B for the max backward")
         if out is None:
             out = torch.empty((self.M, N), dtype=torch.float32, device=self.device)
         else:
@@ -419,12 +428,14 @@ class SparseAdj:
         with torch.cuda.device(self.device):
             spmm_maxpool_backward(self.plan, self.col.data_ptr(),
                                   None if self.val is None else self.val.data_ptr(),
+                                  None if B is None else B.data_ptr(),
                                   argmax.data_ptr(), grad.data_ptr(), N, out.data_ptr(), stream)
         return out
 
-    def backward(self, grad, reduce: str = "sum", argmax=None):
+    def backward(self, grad, reduce: str = "sum", argmax=None, B=None):
         """Gradient with respect to B of ``self.reduce(B, reduce)`` given dC.
-        The transposes are built on first use and kept."""
+        The max needs the forward's argmax and, for a weighted A, its B. The
+        transposes are built on first use and kept."""
         if reduce not in REDUCE:
             raise ValueError(f"unknown reduce {reduce!r}")
         if reduce == "mean":
@@ -437,7 +448,7 @@ class SparseAdj:
             return self._t.reduce(grad, "sum")
         if argmax is None:
             raise ValueError("the max backward needs the forward's argmax")
-        return self._t.maxpool_backward(argmax, grad)
+        return self._t.maxpool_backward(argmax, grad, B=B)
 
     def close(self) -> None:
         for t in (getattr(self, "_t", None), getattr(self, "_tmean", None)):

@@ -683,7 +683,10 @@ spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split) 
     if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_BLOCK) return SPMM_ERR_INVALID_ARG;
     Plan *p = reinterpret_cast<Plan *>(plan);
     p->family_override = family;
-    const int64_t want = t_split > 0 ? t_split : p->t_split_default;
+    // The kernels compare row lengths against a 32-bit threshold; no row is
+    // longer than INT32_MAX entries, so a larger threshold means the same:
+    // split nothing.
+    const int64_t want = t_split > 0 ? std::min<int64_t>(t_split, INT32_MAX) : p->t_split_default;
     if (want == p->t_split) return SPMM_OK;
     cudaError_t e = cudaDeviceSynchronize();   // the workspace and tables may be in use
     if (e != cudaSuccess) return from_cuda(e);

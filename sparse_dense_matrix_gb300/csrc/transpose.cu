@@ -10,7 +10,8 @@
 // atomics), then a gather of rows and values and the new row pointers. Stable
 // on CSR order means the entries of a column come out in increasing row.
 // spmm_maxpool_backward reduces, for every column j of A, dC[i, k] * a_ij over
-// the entries (i, j) whose row chose j as argmax[i, k].
+// the entries (i, j) whose row chose j as argmax[i, k], one stored copy (the
+// one whose product won) per duplicated pair.
 #include <vector>
 
 #include "common.cuh"
@@ -180,20 +181,57 @@ __global__ void k_bounds(const uint32_t *keys, int64_t nnz, int64_t K, int32_t *
 }
 
 // ------------------------------------------------------ max-pool backward
-// Row j of A^T lists the entries (i, a_ij) of column j of A in increasing i.
-// dB[j, c] = sum over them of a_ij * dC[i, c] where argmax[i, c] == j,
-// accumulated in fp32 in that order. L lanes own a row, V columns per lane
-// per step; a warp holds 32 / L rows. Rows of A^T longer than t_split (hub
-// columns of A) are left to the split below, as in the forward product.
+// Row j of A^T lists the entries (i, a_ij) of column j of A in increasing i;
+// copies of a duplicated pair (i, j) are adjacent, in their CSR order. The
+// forward maximum of row i took its value from one stored entry, so for each
+// run of copies of one i only the copy with the largest fp32 product
+// a * B[j, c] (the first on equal products) passes the gradient:
+// dB[j, c] = sum over the runs with argmax[i, c] == j of a_w * dC[i, c],
+// accumulated in fp32 in increasing i (graph-spmm card, "Correctness":
+// duplicated pairs are legal CSR; "API": the argmax feeds this backward).
+// L lanes own a row, V columns per lane per step; a warp holds 32 / L rows.
+// Rows of A^T longer than t_split (hub columns of A) are left to the split
+// below, as in the forward product.
+//
+// mp_accumulate covers entries [p0, p1) of row j, which spans [r0, r1). A run
+// that began before p0 belongs to the previous chunk and is skipped; a run
+// that reaches p1 is followed to its end. bj: B[j, c .. c + V) (weighted A).
 template <int V, bool HAS_VAL>
 __device__ __forceinline__ void mp_accumulate(const int32_t *__restrict__ colT,
                                               const float *__restrict__ valT,
                                               const int32_t *__restrict__ argmax,
                                               const float *__restrict__ dC, int64_t N, int j,
-                                              int p0, int p1, int64_t c, float (&acc)[V]) {
-    for (int p = p0; p < p1; ++p) {
+                                              int r0, int p0, int p1, int r1, int64_t c,
+                                              const float (&bj)[V], float (&acc)[V]) {
+    int p = p0;
+    if (p > r0 && p < p1) {
+        const int prev = colT[p - 1];
+        while (p < p1 && colT[p] == prev) ++p;
+    }
+    while (p < p1) {
         const int64_t i = colT[p];
-        const float a = HAS_VAL ? valT[p] : 1.0f;
+        float aw[V];
+        {
+            const float a = HAS_VAL ? valT[p] : 1.0f;
+#pragma unroll
+            for (int e = 0; e < V; ++e) aw[e] = a;
+        }
+        int q = p + 1;
+        if constexpr (HAS_VAL) {
+            float yw[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) yw[e] = __fmul_rn(aw[e], bj[e]);
+            for (; q < r1 && colT[q] == (int)i; ++q) {
+                const float a = valT[q];
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const float y = __fmul_rn(a, bj[e]);
+                    if (y > yw[e]) { yw[e] = y; aw[e] = a; }
+                }
+            }
+        } else {
+            while (q < r1 && colT[q] == (int)i) ++q;
+        }
         float g[V];
         int w[V];
         if constexpr (V == 4) {
@@ -207,14 +245,24 @@ __device__ __forceinline__ void mp_accumulate(const int32_t *__restrict__ colT,
         }
 #pragma unroll
         for (int e = 0; e < V; ++e)
-            if (w[e] == j) acc[e] = HAS_VAL ? __fmaf_rn(a, g[e], acc[e]) : __fadd_rn(acc[e], g[e]);
+            if (w[e] == j) acc[e] = HAS_VAL ? __fmaf_rn(aw[e], g[e], acc[e]) : __fadd_rn(acc[e], g[e]);
+        p = q;
     }
+}
+
+template <int V, bool HAS_VAL>
+__device__ __forceinline__ void mp_brow(const float *__restrict__ B, int64_t N, int64_t j,
+                                        int64_t c, float (&bj)[V]) {
+#pragma unroll
+    for (int e = 0; e < V; ++e) bj[e] = 0.0f;
+    if constexpr (HAS_VAL) ld_vec<V>(B + j * N + c, bj);
 }
 
 template <int V, bool HAS_VAL>
 __global__ void __launch_bounds__(256) k_maxpool_bwd(const int32_t *__restrict__ rowptrT,
                                                     const int32_t *__restrict__ colT,
                                                     const float *__restrict__ valT,
+                                                    const float *__restrict__ B,
                                                     const int32_t *__restrict__ argmax,
                                                     const float *__restrict__ dC, int64_t rows,
                                                     int64_t N, int lanes, int t_split,
@@ -227,10 +275,11 @@ __global__ void __launch_bounds__(256) k_maxpool_bwd(const int32_t *__restrict__
     const int p0 = rowptrT[j], p1 = rowptrT[j + 1];
     if (p1 - p0 > t_split) return;                 // a split row
     for (int64_t c = (int64_t)sub * V; c < N; c += (int64_t)lanes * V) {
-        float acc[V];
+        float acc[V], bj[V];
 #pragma unroll
         for (int e = 0; e < V; ++e) acc[e] = 0.0f;
-        mp_accumulate<V, HAS_VAL>(colT, valT, argmax, dC, N, (int)j, p0, p1, c, acc);
+        mp_brow<V, HAS_VAL>(B, N, j, c, bj);
+        mp_accumulate<V, HAS_VAL>(colT, valT, argmax, dC, N, (int)j, p0, p0, p1, p1, c, bj, acc);
         st_vec<V>(dB + j * N + c, acc);
     }
 }
@@ -241,6 +290,7 @@ template <int V, bool HAS_VAL>
 __global__ void __launch_bounds__(256) k_maxpool_chunks(const int32_t *__restrict__ rowptrT,
                                                        const int32_t *__restrict__ colT,
                                                        const float *__restrict__ valT,
+                                                       const float *__restrict__ B,
                                                        const int32_t *__restrict__ argmax,
                                                        const float *__restrict__ dC, int64_t N,
                                                        const int2 *__restrict__ chunks,
@@ -250,12 +300,14 @@ __global__ void __launch_bounds__(256) k_maxpool_chunks(const int32_t *__restric
     const int64_t q = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (q >= n_chunks) return;
     const int2 ch = chunks[q];                      // (row of A^T, first entry)
-    const int p1 = min(ch.y + chunk, rowptrT[ch.x + 1]);
+    const int r0 = rowptrT[ch.x], r1 = rowptrT[ch.x + 1];
+    const int p1 = min(ch.y + chunk, r1);
     for (int64_t c = (int64_t)lane * V; c < N; c += 32 * V) {
-        float acc[V];
+        float acc[V], bj[V];
 #pragma unroll
         for (int e = 0; e < V; ++e) acc[e] = 0.0f;
-        mp_accumulate<V, HAS_VAL>(colT, valT, argmax, dC, N, ch.x, ch.y, p1, c, acc);
+        mp_brow<V, HAS_VAL>(B, N, ch.x, c, bj);
+        mp_accumulate<V, HAS_VAL>(colT, valT, argmax, dC, N, ch.x, r0, ch.y, p1, r1, c, bj, acc);
         st_vec<V>(ws + q * N + c, acc);
     }
 }
@@ -397,8 +449,8 @@ spmm_status spmm_transpose(spmm_plan_t plan, const int32_t *col, const float *va
 }
 
 spmm_status spmm_maxpool_backward(spmm_plan_t planT, const int32_t *colT, const float *valT,
-                                  const int32_t *argmax, const float *dC, int64_t N, float *dB,
-                                  void *stream) {
+                                  const float *B, const int32_t *argmax, const float *dC,
+                                  int64_t N, float *dB, void *stream) {
     using namespace spmm;
     if (!planT || N < 0) return SPMM_ERR_INVALID_ARG;
     const Plan *p = reinterpret_cast<const Plan *>(planT);
@@ -406,9 +458,10 @@ spmm_status spmm_maxpool_backward(spmm_plan_t planT, const int32_t *colT, const 
     if (rows == 0 || N == 0) return SPMM_OK;
     if (!dB) return SPMM_ERR_INVALID_ARG;
     if (p->nnz > 0 && (!colT || !argmax || !dC)) return SPMM_ERR_INVALID_ARG;
+    if (p->nnz > 0 && valT && !B) return SPMM_ERR_INVALID_ARG;
     if (N >= INT32_MAX / 4) return SPMM_ERR_UNSUPPORTED;
     const bool v4 = N % 4 == 0 && (uintptr_t)dC % 16 == 0 && (uintptr_t)argmax % 16 == 0 &&
-                    (uintptr_t)dB % 16 == 0;
+                    (uintptr_t)dB % 16 == 0 && (uintptr_t)B % 16 == 0;
     const int V = v4 ? 4 : 1;
     int lanes = 1;
     while (lanes < 32 && (int64_t)lanes * V < N) lanes <<= 1;
@@ -423,11 +476,11 @@ spmm_status spmm_maxpool_backward(spmm_plan_t planT, const int32_t *colT, const 
     }
     const int ts = (int)std::min<int64_t>(p->t_split, INT32_MAX);
     if (v4) {
-        if (hv) k_maxpool_bwd<4, true><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, ts, dB);
-        else k_maxpool_bwd<4, false><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, ts, dB);
+        if (hv) k_maxpool_bwd<4, true><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, B, argmax, dC, rows, N, lanes, ts, dB);
+        else k_maxpool_bwd<4, false><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, B, argmax, dC, rows, N, lanes, ts, dB);
     } else {
-        if (hv) k_maxpool_bwd<1, true><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, ts, dB);
-        else k_maxpool_bwd<1, false><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, rows, N, lanes, ts, dB);
+        if (hv) k_maxpool_bwd<1, true><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, B, argmax, dC, rows, N, lanes, ts, dB);
+        else k_maxpool_bwd<1, false><<<(unsigned)blocks, 256, 0, s>>>(p->rowptr, colT, valT, B, argmax, dC, rows, N, lanes, ts, dB);
     }
     count_launch();
     cudaError_t e = cudaGetLastError();
@@ -436,12 +489,12 @@ spmm_status spmm_maxpool_backward(spmm_plan_t planT, const int32_t *colT, const 
         const unsigned cb = (unsigned)((p->n_chunks + 7) / 8), hb = (unsigned)((p->n_heavy + 7) / 8);
         const int ch = (int)p->chunk;
         if (v4) {
-            if (hv) k_maxpool_chunks<4, true><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
-            else k_maxpool_chunks<4, false><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
+            if (hv) k_maxpool_chunks<4, true><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, B, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
+            else k_maxpool_chunks<4, false><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, B, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
             k_maxpool_combine<4><<<hb, 256, 0, s>>>(p->heavy_rows, p->heavy_chunk0, p->n_heavy, N, ws, dB);
         } else {
-            if (hv) k_maxpool_chunks<1, true><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
-            else k_maxpool_chunks<1, false><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
+            if (hv) k_maxpool_chunks<1, true><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, B, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
+            else k_maxpool_chunks<1, false><<<cb, 256, 0, s>>>(p->rowptr, colT, valT, B, argmax, dC, N, p->chunks, p->n_chunks, ch, ws);
             k_maxpool_combine<1><<<hb, 256, 0, s>>>(p->heavy_rows, p->heavy_chunk0, p->n_heavy, N, ws, dB);
         }
         count_launch(2);

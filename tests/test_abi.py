@@ -62,8 +62,8 @@ def test_host_argument_checks(sdm):
     assert lib.spmm_transpose(None, None, None, 0, None, None, None, None) == 1
     assert lib.spmm_check_wait_timeout(None, 1000, None) == 1
     assert lib.spmm_check_wait_timeout(ctypes.c_void_p(16), 0, None) == 1
-    assert lib.spmm_maxpool_backward(None, None, None, None, None, 4, None, None) == 1
-    assert lib.spmm_maxpool_backward(ctypes.c_void_p(16), None, None, None, None, -1, None,
+    assert lib.spmm_maxpool_backward(None, None, None, None, None, None, 4, None, None) == 1
+    assert lib.spmm_maxpool_backward(ctypes.c_void_p(16), None, None, None, None, None, -1, None,
                                      None) == 1
     assert lib.spmm_route(ctypes.byref(info), 4, 7, 1, 152, -1, ctypes.byref(info)) == 1
     assert lib.spmm_route(ctypes.byref(info), -4, 0, 1, 152, -1, ctypes.byref(info)) == 1

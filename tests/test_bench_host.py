@@ -28,3 +28,16 @@ def test_compulsory_bytes_by_hand():
     # rowptr 4 * 2049, col + val 8 * 16384, B 4 * 2048 * 32, C 4 * 2048 * 32
     assert bench.compulsory_bytes(g, 32, "sum") == 8196 + 131072 + 262144 + 262144
     assert bench.compulsory_bytes(g, 32, "max") == 8196 + 131072 + 3 * 262144   # + argmax
+
+
+def test_default_workload_is_the_largest(monkeypatch):
+    """With no flags the bench times the 4M-row Chung-Lu workload at N = 16,
+    64 and 256 with sum, mean and max (no graph is generated here)."""
+    import bench
+    import gen
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    args = bench.parse()
+    assert args.config == 5 and args.gpus == 1 and args.warmup >= 3
+    assert gen.CONFIGS[5]["name"] == "chung_lu_4M"
+    assert bench.DEFAULT_N[5] == (16, 64, 256)
+    assert set(gen.CONFIGS[5]["reduce"]) == {"sum", "mean", "max"}

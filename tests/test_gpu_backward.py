@@ -4,8 +4,10 @@
   transpose (scaled mean values too: both sides divide in fp64 and round once).
 * sum / mean backward: a product with the GPU transpose, held to the forward's
   tolerance 1e-5 * T + 1e-6 against the oracle's product with its own transpose.
-* max-pool backward: 1e-5 * T + 1e-6 with T = sum of |a_ij * dC[i, c]| over the
-  contributing entries (the oracle's backward of |val| and |dC|). The argmax fed
+* max-pool backward: 1e-5 * T + 1e-6 with T = max |a| times the sum of
+  |dC[i, c]| over the rows that chose column j. Duplicated pairs pass the
+  gradient through the one copy whose product won (weighted copies differ; a
+  run of copies can straddle a chunk boundary of a split row). The argmax fed
   to both sides is the oracle's; the GPU's forward argmax is first checked equal.
 """
 import numpy as np
@@ -140,12 +142,15 @@ def check_maxpool(sdm, dev, g, N, seed=0):
     torch.cuda.synchronize()
     _, Ar, _ = oracle.spmm(g.rowptr, g.col, g.val, B, "max")
     assert np.array_equal(A.cpu().numpy(), Ar)
-    got = adj.backward(to_dev(dC, dev), "max", argmax=to_dev(Ar, dev))
+    got = adj.backward(to_dev(dC, dev), "max", argmax=to_dev(Ar, dev),
+                       B=None if g.val is None else to_dev(B, dev))
     torch.cuda.synchronize()
     got = got.cpu().numpy()
-    want = oracle.maxpool_backward(g.rowptr, g.col, g.val, Ar, dC, g.K)
-    T = oracle.maxpool_backward(g.rowptr, g.col, None if g.val is None else np.abs(g.val), Ar,
-                                np.abs(dC), g.K)
+    want = oracle.maxpool_backward(g.rowptr, g.col, g.val, Ar, dC, g.K, B)
+    # scale of the tolerance: max |a| times the sum of |dC[i, c]| over the rows
+    # that chose j (a bound of the sum of |a_w * dC[i, c]|)
+    amax = 1.0 if g.val is None or g.nnz == 0 else float(np.abs(g.val).max())
+    T = oracle.maxpool_backward(g.rowptr, g.col, None, Ar, np.abs(dC), g.K) * amax
     err = np.abs(got.astype(np.float64) - want.astype(np.float64))
     bound = RTOL * T.astype(np.float64) + ATOL
     assert not (err > bound).any(), f"{g.name} N={N}: {int((err > bound).sum())} outside tolerance"
@@ -171,6 +176,25 @@ def test_maxpool_backward_split_rows(sdm, cuda_device):
     t.close()
     adj.close()
     check_maxpool(sdm, cuda_device, g, 16)
+
+
+def test_maxpool_backward_duplicates_across_chunks(sdm, cuda_device):
+    """Copies of one pair (i, 7) placed so that every chunk boundary of the
+    split row 7 of A^T falls inside a run of copies (runs of 3 copies with
+    distinct weights): each run must count once, in the chunk where it starts."""
+    M, K = 4000, 50
+    rng = np.random.default_rng(21)
+    rows = [[7, 7, 7] + rng.integers(0, K, size=2).tolist() for _ in range(M)]
+    vals = [rng.standard_normal(len(r)).astype(np.float32).tolist() for r in rows]
+    g = gen.from_rows("runs", M, K, rows, vals)
+    adj = make_adj(sdm, g, cuda_device)
+    t = adj.transpose()
+    info = t.describe(16)
+    assert info["n_heavy"] >= 1 and info["chunk"] % 3 != 0
+    t.close()
+    adj.close()
+    check_maxpool(sdm, cuda_device, g, 16)
+    check_maxpool(sdm, cuda_device, gen.from_rows("runs_u", M, K, rows, None), 16)
 
 
 def test_maxpool_backward_deterministic(sdm, cuda_device):

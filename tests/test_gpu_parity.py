@@ -67,6 +67,21 @@ def test_forced_families_and_splits(sdm, cuda_device, family, t_split, N):
         compare(g, B, red, C, A, label=f"{family} t={t_split} N={N} {red}")
 
 
+@pytest.mark.parametrize("family", ["rowgroup", "warprow"])
+def test_split_threshold_beyond_int32(sdm, cuda_device, family):
+    """A threshold above INT32_MAX splits nothing; every row is still written."""
+    g = small("rmat")
+    B = gen.features(g.K, 16, seed=8)
+    adj = make_adj(sdm, g, cuda_device)
+    adj.set_family(family, 1 << 40)
+    info = adj.describe(16)
+    assert info["t_split"] == 2**31 - 1 and info["n_heavy"] == 0
+    Bd = to_dev(B, cuda_device)
+    for red in ("sum", "mean", "max"):
+        C, A = gpu_reduce(adj, Bd, red)
+        compare(g, B, red, C, A, label=f"{family} t=2^40 {red}")
+
+
 @pytest.mark.parametrize("t_split", [0, 24])
 @pytest.mark.parametrize("N", [128, 132, 256, 384, 520, 1040])
 def test_coltile_family(sdm, cuda_device, t_split, N):

@@ -1,13 +1,16 @@
 """spmm_run_noalloc: the product without a plan and without device allocation,
 for callers whose device memory belongs to another allocator or who must not
-allocate after start-up. Checked against the planned entry point (spmm_run
-through SparseAdj) on consecutive calls, which share the library's one static
-scratch array. This file is collected last on purpose."""
+allocate after start-up. Checked element by element against the oracle (the
+same tolerance and bit-exact max/argmax as every other parity test) on
+consecutive calls, which share the library's one static scratch array, and
+cross-checked against the planned entry point (spmm_run through SparseAdj).
+After a first call, further calls must leave the device's free memory
+unchanged. This file is collected last on purpose."""
 import numpy as np
 import pytest
 
 import gen
-from parity_util import ATOL, RTOL, make_adj, to_dev
+from parity_util import ATOL, RTOL, compare, make_adj, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +44,7 @@ def _planned(sdm, adj, Bd, red):
     return r.cpu().numpy(), None
 
 
-def test_noalloc_matches_planned_entry_point_on_consecutive_calls(sdm, cuda_device):
+def test_noalloc_matches_oracle_on_consecutive_calls(sdm, cuda_device):
     import oracle
     g = gen.rmat(scale=13, edge_factor=16, seed=4)
     deg = g.degrees()
@@ -49,10 +52,13 @@ def test_noalloc_matches_planned_entry_point_on_consecutive_calls(sdm, cuda_devi
     assert (deg > t_split).any()                  # the split path and its scratch are used
     adj = make_adj(sdm, g, cuda_device)
     n0 = sdm.spmm_launch_count()
-    for N, red in ((32, "sum"), (64, "max"), (32, "mean")):
+    for N, red in ((32, "sum"), (64, "max"), (32, "mean"), (64, "max")):
         B = gen.features(g.K, N, seed=N + 11)
         Bd = to_dev(B, cuda_device)
         C1, A1 = _noalloc(sdm, g, cuda_device, Bd, red)
+        compare(g, B, red, C1, A1, label=f"noalloc N={N} {red}")
+        # the planned entry point on the same input: max bit for bit, the sums
+        # both within the oracle's tolerance, hence within twice it of each other
         C0, A0 = _planned(sdm, adj, Bd, red)
         if red == "max":
             assert np.array_equal(C1.view(np.int32), C0.view(np.int32))
@@ -62,6 +68,37 @@ def test_noalloc_matches_planned_entry_point_on_consecutive_calls(sdm, cuda_devi
             err = np.abs(C1.astype(np.float64) - C0.astype(np.float64))
             assert np.all(err <= 2 * (RTOL * T.astype(np.float64) + ATOL)), red
     assert sdm.spmm_launch_count() > n0
+    adj.close()
+
+
+def test_noalloc_allocates_nothing(sdm, cuda_device):
+    """Once the library is loaded and the array's address looked up (the first
+    call), calls change neither the device's free memory nor torch's."""
+    import torch
+    g = gen.chung_lu(1 << 14, 2.1, 25.0, 2000.0, seed=3)
+    N = 64
+    B = gen.features(g.K, N, seed=5)
+    rp, cl, vl = to_dev(g.rowptr, cuda_device), to_dev(g.col, cuda_device), to_dev(g.val, cuda_device)
+    Bd = to_dev(B, cuda_device)
+    C = torch.empty((g.M, N), dtype=torch.float32, device=cuda_device)
+    A = torch.empty((g.M, N), dtype=torch.int32, device=cuda_device)
+
+    def call(red):
+        sdm.spmm_run_noalloc(rp.data_ptr(), cl.data_ptr(), vl.data_ptr(), Bd.data_ptr(), g.M,
+                             g.K, N, sdm.REDUCE[red], C.data_ptr(),
+                             A.data_ptr() if red == "max" else None)
+
+    call("sum")
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(cuda_device)
+    torch0 = torch.cuda.memory_reserved(cuda_device)
+    for red in ("sum", "max", "mean", "sum"):
+        call(red)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(cuda_device)
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
+    assert torch.cuda.memory_reserved(cuda_device) == torch0
+    compare(g, B, "sum", C.cpu().numpy(), None, label="noalloc after the memory check")
 
 
 def test_noalloc_rejects_inputs_beyond_its_scratch(sdm, cuda_device):
@@ -76,11 +113,7 @@ def test_noalloc_rejects_inputs_beyond_its_scratch(sdm, cuda_device):
         _noalloc(sdm, g, cuda_device, Bd, "sum")
     assert e.value.status == 5                    # SPMM_ERR_UNSUPPORTED
     # a size that fits still works after the refusal
-    import oracle
     B = gen.features(K, 8, seed=1)
     Bd = to_dev(B, cuda_device)
     C1, _ = _noalloc(sdm, g, cuda_device, Bd, "sum")
-    C0, _ = _planned(sdm, make_adj(sdm, g, cuda_device), Bd, "sum")
-    _, _, T = oracle.spmm(g.rowptr, g.col, g.val, B, "sum")
-    err = np.abs(C1.astype(np.float64) - C0.astype(np.float64))
-    assert np.all(err <= 2 * (RTOL * T.astype(np.float64) + ATOL))
+    compare(g, B, "sum", C1, None, label="noalloc after a refusal")
