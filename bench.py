@@ -99,7 +99,8 @@ def parse():
     ap.add_argument("--config", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--family", default="auto",
-                    choices=["auto", "rowgroup", "warprow", "coltile", "window", "block"])
+                    choices=["auto", "rowgroup", "warprow", "coltile", "window", "block",
+                             "segment"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds of oracle work for the whole --impl reference run")

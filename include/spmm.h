@@ -63,12 +63,22 @@ typedef enum {
     SPMM_FAMILY_WINDOW = 3,    /* persistent CTAs over contiguous row ranges; the B rows of a
                                   sliding window [r0 - W, r1 + W) are streamed into shared
                                   memory by bulk copies (column-locality graphs)           */
-    SPMM_FAMILY_BLOCK = 4      /* block-diagonal graphs: each 128-row tile's 256-column
-                                  diagonal block is densified and multiplied on the tensor
-                                  cores (split TF32, fp32 accumulation); the entries outside
-                                  the block are added by the same CTA. Sum and mean, N % 16
-                                  == 0, aligned B and C. Used only when pinned with
-                                  spmm_plan_set_family (the router does not choose it)     */
+    SPMM_FAMILY_BLOCK = 4,     /* block-diagonal graphs: each 128-row tile's 256-column
+                                  diagonal block, densified and split into TF32 hi + lo once
+                                  per plan (spmm_plan_prepare_blocks), is multiplied on the
+                                  tensor cores (fp32 accumulation); the entries outside the
+                                  block, also prepared, are added by the same CTA. Sum and
+                                  mean, N % 16 == 0, aligned B and C, a plan of whole rows
+                                  (not a row range)                                          */
+    SPMM_FAMILY_SEGMENT = 5    /* skewed graphs without column locality: the CSR traversal is
+                                  cut into equal merge-path tiles of entries plus row ends
+                                  (ParamSpMM section 3.2, nonzero-split balancing); each warp
+                                  streams its tiles' rowptr/col/val into shared memory with
+                                  bulk copies and reduces them in lane-group slices, rows
+                                  open across tiles carried in registers, the few rows open
+                                  at the ends of a warp's range combined by a second launch.
+                                  N % 4 == 0, 16-byte aligned B, C, argmax, col and val;
+                                  long rows need no separate split                          */
 } spmm_family;
 
 typedef struct spmm_plan_s *spmm_plan_t;
@@ -112,6 +122,14 @@ typedef struct {
     int64_t blk_intra;      /* entries with col / 256 == row / 256 (diagonal blocks)     */
     /* row-range plans (spmm_plan_create_range): global index of the plan's row 0 */
     int64_t row0;
+    /* SEGMENT family: merge-path tiles of the plan (descriptor), and for the
+       queried (N, reduce) the warps of the grid and the four-column chunks per lane */
+    int64_t seg_tiles;
+    int32_t seg_warps;
+    int32_t seg_chunks;
+    /* BLOCK family: device bytes of the plan's prepared diagonal blocks and
+       off-block entries (0 until prepared) */
+    int64_t block_bytes;
 } spmm_plan_info;
 
 /*
@@ -238,6 +256,27 @@ spmm_status spmm_plan_reserve(spmm_plan_t plan, int64_t N, spmm_reduce reduce);
 spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *stream);
 
 /*
+ * spmm_plan_prepare_blocks -- the BLOCK family's per-plan preparation (RA-SpMM,
+ * "tensor-core SpMM with per-matrix preprocessing": A is fixed, so its dense
+ * blocks are built once and reused by every product). For every 128-row tile
+ * the 256-column diagonal block is densified (duplicates added in CSR order,
+ * fp32) and split into TF32 hi and lo operand pieces in the tensor cores'
+ * layout; the entries outside the diagonal blocks are copied, in CSR order,
+ * into a compact CSR. Plan-owned device memory: 256 KB per 128-row tile plus
+ * 4 (M + 1) + 8 (4 unweighted) bytes per outside entry (spmm_plan_info's
+ * block_bytes).
+ *   col, val : device, the plan's graph (as for spmm_run; val NULL when A is
+ *              unweighted). The pieces are a copy: after changing col or val,
+ *              prepare again.
+ * spmm_run prepares on first use of the BLOCK family (and again when the
+ * flavour of A, weighted or not, changes), so this call only moves that cost
+ * out of the first product. Synchronous. SPMM_ERR_UNSUPPORTED for a
+ * row-range plan; SPMM_ERR_OOM when the device is full.
+ */
+spmm_status spmm_plan_prepare_blocks(spmm_plan_t plan, const int32_t *col, const float *val,
+                                     void *stream);
+
+/*
  * spmm_plan_sync -- wait for `stream`, then report any error a kernel of this
  * plan recorded on the device (SPMM_ERR_TIMEOUT when a bounded wait gave up)
  * and clear it. Synchronous.
@@ -295,11 +334,12 @@ int64_t spmm_default_t_split(int64_t M, int64_t nnz, int num_sms);
  * spmm_default_t_split(M, nnz, SMs) are split into chunks whose partials go to
  * a file-scope device array of 64 MiB that every GPU which loads the library
  * holds until the process exits. At most 65,536 split rows, 262,144 chunks and
- * chunks x N x 4 bytes of partials (x 2 for SPMM_MAX) up to about 61 MiB fit
+ * chunks x N x 4 bytes of partials (x 2 for SPMM_MAX) up to about 60 MiB fit
  * in it; larger inputs return SPMM_ERR_UNSUPPORTED before any product kernel
  * runs. rowptr[0] != 0 or a decreasing rowptr returns SPMM_ERR_INVALID_INPUT.
  * Partly synchronous: nnz and the split-row counts are read back to the host
- * (draining `stream`) before the product is enqueued.
+ * (draining `stream`) before the product is enqueued. The split rows are found
+ * by three small launches over blocks of at least 4,096 rows.
  * The first call on a device looks up the array's device address with
  * cudaGetSymbolAddress; make that first call before any stream capture.
  * Every call shares the one array and it keeps the last call's contents:

@@ -32,12 +32,14 @@ __all__ = [
     "spmm_route", "spmm_default_t_split", "spmm_status_string", "spmm_launch_count",
     "spmm_run_noalloc", "spmm_transpose", "spmm_maxpool_backward", "spmm_run_ex", "ACT",
     "spmm_check_wait_timeout", "spmm_plan_create_range", "spmm_partition_rows",
+    "spmm_plan_prepare_blocks",
     "PlanInfo", "REDUCE", "FAMILY", "lib", "build_library",
 ]
 
 REDUCE = {"sum": 0, "mean": 1, "max": 2}
 ACT = {None: 0, "none": 0, "relu": 1}
-FAMILY = {"auto": -1, "rowgroup": 0, "warprow": 1, "coltile": 2, "window": 3, "block": 4}
+FAMILY = {"auto": -1, "rowgroup": 0, "warprow": 1, "coltile": 2, "window": 3, "block": 4,
+          "segment": 5}
 STATUS = {0: "SPMM_OK", 1: "SPMM_ERR_INVALID_ARG", 2: "SPMM_ERR_INVALID_INPUT", 3: "SPMM_ERR_OOM",
           4: "SPMM_ERR_CUDA", 5: "SPMM_ERR_UNSUPPORTED", 6: "SPMM_ERR_TIMEOUT"}
 
@@ -58,6 +60,8 @@ class PlanInfo(ctypes.Structure):
         ("window_smem", ctypes.c_int64), ("window_chunks", ctypes.c_int32),
         ("rows_sorted", ctypes.c_int32), ("blk_intra", ctypes.c_int64),
         ("row0", ctypes.c_int64),
+        ("seg_tiles", ctypes.c_int64), ("seg_warps", ctypes.c_int32),
+        ("seg_chunks", ctypes.c_int32), ("block_bytes", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
@@ -90,6 +94,7 @@ def _load():
         "spmm_plan_reserve": ([vp, i64, i32], i32),
         "spmm_plan_validate_cols": ([vp, vp, vp], i32),
         "spmm_plan_sync": ([vp, vp], i32),
+        "spmm_plan_prepare_blocks": ([vp, vp, vp, vp], i32),
         "spmm_plan_describe": ([vp, i64, i32, P(PlanInfo)], i32),
         "spmm_plan_set_family": ([vp, i32, i64], i32),
         "spmm_route": ([P(PlanInfo), i64, i32, i32, i32, i32, P(PlanInfo)], i32),
@@ -193,6 +198,13 @@ def spmm_plan_validate_cols(plan: int, col_ptr: int, stream=None) -> None:
            "spmm_plan_validate_cols")
 
 
+def spmm_plan_prepare_blocks(plan: int, col_ptr: int, val_ptr, stream=None) -> None:
+    """The BLOCK family's per-plan preparation (dense diagonal blocks split
+    into TF32 hi/lo, and the entries outside them); synchronous."""
+    _check(lib.spmm_plan_prepare_blocks(plan, col_ptr, val_ptr, _stream_handle(stream)),
+           "spmm_plan_prepare_blocks")
+
+
 def spmm_plan_sync(plan: int, stream=None) -> None:
     _check(lib.spmm_plan_sync(plan, _stream_handle(stream)), "spmm_plan_sync")
 
@@ -221,7 +233,7 @@ def spmm_route(desc: dict, N: int, reduce: int, aligned: int = 3, num_sms: int =
     d = PlanInfo()
     for k in ("M", "K", "nnz", "d_max", "n_empty", "dbar", "cv", "t_split", "chunk",
               "n_heavy", "n_chunks", "band_w", "band_cover", "rows_sorted", "blk_intra",
-              "row0"):
+              "row0", "seg_tiles"):
         if k in desc:
             setattr(d, k, desc[k])
     out = PlanInfo()

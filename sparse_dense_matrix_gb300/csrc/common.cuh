@@ -16,6 +16,18 @@ namespace spmm {
 constexpr int kWarp = 32;
 constexpr int kMaxTilesY = 65535;
 constexpr int kBlockRows = 256;     // diagonal block of the BLOCK (tensor-core) family
+// SEGMENT family: merge-path items (stored entries + row ends) per tile, and
+// warps per CTA. 544 = 17 * 32, so that the G lane groups of a warp, whose
+// slices start 544 / G items apart, read different shared-memory banks when a
+// tile lies inside one long row.
+#ifndef SPMM_SEG_ITEMS
+#define SPMM_SEG_ITEMS 544
+#endif
+#ifndef SPMM_SEG_WARPS
+#define SPMM_SEG_WARPS 16
+#endif
+constexpr int kSegItems = SPMM_SEG_ITEMS;
+constexpr int kSegWarps = SPMM_SEG_WARPS;
 
 // Everything a plan owns. Host-side object; the pointers are device memory.
 struct Plan {
@@ -44,6 +56,21 @@ struct Plan {
     // workspace for chunk partials: [n_chunks][N] fp32 (+ int32 for max)
     void *work = nullptr;
     size_t work_bytes = 0;
+
+    // SEGMENT family: merge-path coordinates (rows ended, entries consumed)
+    // of the start of every tile of kSegItems items, [seg_n_tiles + 1]
+    int2 *seg_tiles = nullptr;
+    int64_t seg_n_tiles = 0;
+
+    // BLOCK family, prepared once per plan (block_prepare): every 128-row
+    // tile's diagonal block densified and split into TF32 hi/lo operand
+    // pieces, and a compact CSR of the entries outside the diagonal blocks.
+    // bk_flavor: -1 not prepared, 0 unweighted A, 1 weighted A.
+    void *bk_tiles = nullptr;
+    int32_t *bk_off_rowptr = nullptr, *bk_off_col = nullptr;
+    float *bk_off_val = nullptr;
+    int64_t bk_n_off = 0, bk_bytes = 0;
+    int bk_flavor = -1;
 
     int32_t *err = nullptr;          // device error words, see kErr*
     int family_override = SPMM_FAMILY_AUTO;
@@ -108,6 +135,18 @@ struct RunArgs {
     int32_t mean;                             // 1: a SUM kernel finishes the mean (x 1/d)
     int64_t row0;                             // global index of local row 0 (row-range plans);
                                               // only the WINDOW family's column window uses it
+    // SEGMENT family
+    const int2 *__restrict__ seg_tiles;       // [seg_n_tiles + 1] (rows ended, entries consumed)
+    int64_t seg_n_tiles;
+    int32_t seg_warps;                        // warps of the grid (each owns a range of tiles)
+    float *__restrict__ seg_cval;             // [tiles_y][seg_warps][2][cw] open-row partials
+    int32_t *__restrict__ seg_carg;           // same layout, argmax (max only)
+    int4 *__restrict__ seg_meta;              // [seg_warps] (head row, head ends, tail row, 0)
+    // BLOCK family (the plan's prepared pieces)
+    const void *__restrict__ bk_a;
+    const int32_t *__restrict__ bk_off_rowptr;
+    const int32_t *__restrict__ bk_off_col;
+    const float *__restrict__ bk_off_val;
 };
 
 // Fused epilogue on V consecutive outputs starting at column c: C = act(C + bias).
@@ -277,6 +316,17 @@ cudaError_t launch_window(const RunArgs &a, const WinShape &w, int reduce, bool 
 bool window_shape(int64_t M, int64_t K, int64_t N, double dbar, int64_t W, bool has_val,
                   int lanes, int chunks, int rows_per_group, WinShape *out);
 cudaError_t launch_block(const RunArgs &a, int reduce, bool has_val, cudaStream_t s);
+// BLOCK preparation from the plan's rowptr and the caller's col/val (synchronous)
+cudaError_t block_prepare(Plan *p, const int32_t *col, const float *val, cudaStream_t s);
+void block_free(Plan *p);
+size_t block_prepared_bytes(int64_t M, int64_t n_off, bool has_val);
+// SEGMENT: main kernel (ctas_x x tiles_y CTAs) and the combine of the open rows
+cudaError_t launch_segment(const RunArgs &a, int lanes, int chunks, int reduce, bool has_val,
+                           int tiles_y, cudaStream_t s);
+// workspace bytes of the SEGMENT family's open-row partials for a launch
+size_t segment_workspace(int64_t seg_warps, int64_t tiles_y, int lanes, int chunks, int reduce);
+// warps of a SEGMENT launch on `num_sms` SMs with `tiles_y` column tiles
+int64_t segment_warps(int64_t n_tiles, int num_sms, int64_t tiles_y);
 // grow a plan's workspace to at least `need` bytes (cudaMalloc; synchronous)
 spmm_status plan_ensure_workspace(Plan *p, size_t need);
 

@@ -3,23 +3,32 @@
 // a community graph are dense enough that a dense product on tcgen05 moves far
 // fewer bytes than per-entry gathers).
 //
-// A CTA of 128 threads owns rows [r0, r0 + 128) and output columns
-// [n0, n0 + 128). Its rows lie in one diagonal block of kBlockRows columns,
-// [b0, b0 + kBlockRows). For each chunk of 32 of those columns the CTA
-// densifies A's entries into a 128 x 32 tile (thread t owns row r0 + t;
-// duplicates are added in CSR order), stages B's 32 x 128 slice, and one
-// thread issues tcgen05.mma kind::tf32 into a 128 x 128 fp32 accumulator in
-// tensor memory. fp32 operands are split as x = hi + lo with hi and lo TF32
-// (round to nearest), and each product is hi_a hi_b + hi_a lo_b + lo_a hi_b,
-// about 2^-21 relative per term, inside the fp32 SpMM tolerance (an
-// unweighted A has lo_a = 0, so two passes). Operand tiles are K-major, no
+// A is fixed, so its share of the work is done once per plan
+// (block_prepare): the diagonal block of every 128-row tile (the kBlockRows
+// columns [b0, b0 + kBlockRows) that hold its rows' own community) is
+// densified (duplicates added in CSR order, fp32) and split as x = hi + lo
+// with hi and lo TF32 (round to nearest), stored in the tensor cores' K-major
+// operand layout, one 8 KB piece per 16 block columns; the entries outside
+// the block are copied into a compact CSR of their own. A launch then only
+// streams these pieces:
+//   * warp 0 (one thread) bulk-copies the chunk's A pieces (hi, and lo when A
+//     is weighted) and loads B's 16 x 128 chunk by a 2-D tensor copy, into a
+//     two-stage mbarrier ring;
+//   * warps 4-7 split each B chunk into TF32 hi and lo, transposed into the
+//     K-major layout;
+//   * warp 1 (one thread) issues tcgen05.mma kind::tf32 into a 128 x 128 fp32
+//     accumulator in tensor memory: a_hi b_hi + a_hi b_lo + a_lo b_hi (about
+//     2^-21 relative per term; two passes for an unweighted A, whose lo is 0)
+//     and commits each chunk to the stage's "free" barrier.
+// The three roles overlap across the two stages. The epilogue reads the
+// accumulator back through shared memory and finishes the rows
+// warp-cooperatively: the row's entries outside the block in CSR order (fp32
+// FMA), the mean's 1/d, the fused bias/ReLU, one store of C. Sum and mean only
+// (max needs comparisons, not products). Operand tiles are K-major without
 // swizzle: 8-row x 16-byte core matrices, 128 bytes apart along K and
-// 32 * 4 * 8 bytes apart along rows.
-// The epilogue reads the accumulator back (thread t = TMEM lane t = row r0+t),
-// adds the row's entries outside the diagonal block in CSR order with fp32
-// FMA, applies the mean's 1/d and the fused bias/ReLU, and writes C once.
-// Sum and mean only (max needs comparisons, not products).
+// (KC / 4) * 128 bytes apart along rows.
 #include <cstring>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -30,24 +39,34 @@ namespace spmm {
 
 namespace {
 
-constexpr int kBkThreads = 256;              // warps 0-3: A rows (TMEM lanes 0..127); 4-7: B
+constexpr int kBkThreads = 256;
 constexpr int kBkM = 128;                    // rows per CTA (MMA M)
 constexpr int kBkN = 128;                    // output columns per CTA (MMA N, TMEM columns)
-constexpr int kBkKC = 32;                    // block columns per staged chunk
+constexpr int kBkKC = 16;                    // block columns per chunk
 constexpr int kBkChunks = kBlockRows / kBkKC;
 constexpr uint32_t kLBO = 128;               // next core matrix along K, bytes
 constexpr uint32_t kSBO = (kBkKC / 4) * 128; // next 8-row group, bytes
-constexpr uint32_t kTileA = kBkM * kBkKC * 4;
-constexpr uint32_t kTileB = kBkN * kBkKC * 4;
-constexpr int kBkStages = 2;                 // B chunks in flight (tensor copies)
-constexpr uint32_t kOffStage = 2 * kTileA + 2 * kTileB;
-constexpr uint32_t kOffBars = kOffStage + kBkStages * kBkKC * kBkN * 4;
-constexpr int kBkSmem = (int)kOffBars + 64 + 1024;
+constexpr uint32_t kPiece = kBkM * kBkKC * 4;       // one A piece (8 KB)
+constexpr uint32_t kBTile = kBkN * kBkKC * 4;       // one B operand tile (8 KB)
+constexpr int kBkStages = 2;
+// per stage: A hi, A lo, B as loaded, B hi, B lo
+constexpr uint32_t kStageBytes = 2 * kPiece + 3 * kBTile;
+constexpr uint32_t kOffBars = kBkStages * kStageBytes;
+// the CTA's entries outside the diagonal block, staged during the main loop
+constexpr int kOffCap = 1536;
+constexpr uint32_t kOffORp = kOffBars + 128;                 // int [kBkM + 1]
+constexpr uint32_t kOffOCol = kOffORp + (kBkM + 1 + 3) / 4 * 16;
+constexpr uint32_t kOffOVal = kOffOCol + kOffCap * 4;
+constexpr int kBkSmem = (int)(kOffOVal + kOffCap * 4) + 1024;
 constexpr int kTilePitch = kBkN + 4;         // accumulator rows in shared memory (floats)
-static_assert(kBkM * kTilePitch * 4 <= (int)kOffBars, "the accumulator tile reuses the operand tiles");
+constexpr int kConvThreads = 4 * kWarp;      // warps 4-7
+static_assert(kBkM * kTilePitch * 4 <= (int)kOffBars, "the accumulator tile reuses the stages");
+
+// prepared A: [row tile][chunk][hi, lo][kPiece bytes]
+constexpr size_t kTileBytes = (size_t)kBkChunks * 2 * kPiece;
 
 // byte offset of element (r, k) in a K-major tile of kBkKC columns
-__device__ __forceinline__ uint32_t km_off(int r, int k) {
+__host__ __device__ __forceinline__ uint32_t km_off(int r, int k) {
     return (uint32_t)(r >> 3) * kSBO + (uint32_t)(k >> 2) * kLBO + (uint32_t)(r & 7) * 16u +
            (uint32_t)(k & 3) * 4u;
 }
@@ -95,36 +114,32 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 template <int RED, bool HAS_VAL>
-__global__ void __launch_bounds__(kBkThreads) k_block(const RunArgs a,
+__global__ void __launch_bounds__(kBkThreads, 2) k_block(const RunArgs a,
                                                      const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint32_t *a_hi = reinterpret_cast<uint32_t *>(sm);
-    uint32_t *a_lo = reinterpret_cast<uint32_t *>(sm + kTileA);
-    uint32_t *b_hi = reinterpret_cast<uint32_t *>(sm + 2 * kTileA);
-    uint32_t *b_lo = reinterpret_cast<uint32_t *>(sm + 2 * kTileA + kTileB);
-    float *stage = reinterpret_cast<float *>(sm + kOffStage);        // [kBkStages][KC][kBkN]
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + kOffBars);     // [kBkStages]
-    uint64_t *mma_bar = full + kBkStages;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(mma_bar + 1);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + kOffBars);   // [stage] A + B landed
+    uint64_t *conv = full + kBkStages;                               // [stage] B split
+    uint64_t *done = conv + kBkStages;                               // [stage] MMAs read it
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + kBkStages);
+    auto stage = [&](int s) { return sm + (size_t)s * kStageBytes; };
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int64_t r0 = (int64_t)blockIdx.x * kBkM;
-    const int n0 = blockIdx.y * kBkN;
+    const int n0 = blockIdx.x * kBkN;                     // column tiles vary fastest:
+    const int64_t tile = blockIdx.y;                      // they share the A pieces in L2
+    const int64_t r0 = tile * kBkM;
     const int n_eff = min(kBkN, a.N - n0);                // a multiple of 16
     const int64_t b0 = r0 / kBlockRows * kBlockRows;      // first column of the diagonal block
     const int64_t N = a.N;
-    // warps w and w + 4 share TMEM lanes 32 (w % 4) .. +31: the rows of the tile
-    const int rl = (warp & 3) * 32 + lane;
-    const int64_t row = r0 + rl;
-    const bool has_row = row < a.M;
-    const int p0 = has_row ? a.rowptr[row] : 0;
-    const int p1 = has_row ? a.rowptr[row + 1] : 0;
-    const bool a_side = warp < 4;                         // warps 0-3 densify A, 4-7 convert B
+    const unsigned char *apiece = reinterpret_cast<const unsigned char *>(a.bk_a) +
+                                  (size_t)tile * kTileBytes;
 
     if (t == 0) {
-        for (int st = 0; st < kBkStages; ++st) mbar_init(&full[st], 1);
-        mbar_init(mma_bar, 1);
+        for (int s = 0; s < kBkStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&conv[s], kConvThreads / kWarp);
+            mbar_init(&done[s], 1);
+        }
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -138,114 +153,35 @@ __global__ void __launch_bounds__(kBkThreads) k_block(const RunArgs a,
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tslot;
-    const uint32_t id = instr_desc(kBkM, n_eff);
     constexpr int kPasses = HAS_VAL ? 3 : 2;
-    constexpr uint32_t kStageBytes = kBkKC * kBkN * 4;
+    constexpr uint32_t kLoadBytes = (HAS_VAL ? 2 : 1) * kPiece + kBTile;
 
-    // B chunks come by 2-D tensor copies (rows past K and columns past N read
-    // as zeros), kBkStages ahead of their conversion
-    const int tma_thread = 4 * kWarp;
-    int issued = 0, converted = 0;        // chunks requested / taken from the staging ring
-    if (t == tma_thread) {
-        for (int kc = 0; kc < kBkStages && kc < kBkChunks; ++kc, ++issued) {
-            mbar_arrive_expect_tx(&full[kc], kStageBytes);
-            tensor2d_g2s(stage + (size_t)kc * kBkKC * kBkN, &bmap, n0, (int)(b0 + kc * kBkKC),
-                         &full[kc]);
-        }
-    }
-
-    // Sorted rows: the entries of the block are [qa, qb). They are read through
-    // an 8-entry register buffer (jb, wb) refilled by 8 independent loads, and
-    // consumed in order (a prefix of the buffer per chunk).
-    int q = p0, qa = p0, nb = 0, cons = 0;
-    int jb[8];
-    float wb[8];
-    auto refill = [&]() {
-        q += nb;
-        nb = min(8, p1 - q);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            jb[u] = u < nb ? __ldg(a.col + q + u) : INT_MAX;
-            wb[u] = (HAS_VAL && u < nb) ? __ldg(a.val + q + u) : 1.0f;
-        }
-        cons = 0;
-    };
-    if (a_side && a.rows_sorted) {
-        while (q < p1 && (int64_t)a.col[q] < b0) ++q;
-        qa = q;
-        refill();
-    }
     bool ok = true;
-    for (int kc = 0; kc < kBkChunks && ok; ++kc) {
-        const int64_t c0 = b0 + (int64_t)kc * kBkKC;
-        const int st = kc % kBkStages;
-        if (a_side) {
-            // ---- A: this thread's row; fp32 sums staged in the lo tile, then split
-            float *tmp = reinterpret_cast<float *>(a_lo);
-#pragma unroll
-            for (int k4 = 0; k4 < kBkKC / 4; ++k4)
-                *reinterpret_cast<float4 *>(tmp + (km_off(rl, 4 * k4) >> 2)) = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (a.rows_sorted) {
-                while (nb > 0) {
-                    int used = cons;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        if (u >= cons && u < nb && (int64_t)jb[u] < c0 + kBkKC) {
-                            tmp[km_off(rl, (int)((int64_t)jb[u] - c0)) >> 2] += wb[u];
-                            used = u + 1;
-                        }
-                    }
-                    cons = used;
-                    if (cons < nb) break;             // the rest belongs to later chunks
-                    refill();
-                }
-            } else {
-                for (int p = p0; p < p1; ++p) {
-                    const int64_t c = a.col[p];
-                    if ((uint64_t)(c - c0) < (uint64_t)kBkKC)
-                        tmp[km_off(rl, (int)(c - c0)) >> 2] += HAS_VAL ? a.val[p] : 1.0f;
-                }
-            }
-#pragma unroll
-            for (int k4 = 0; k4 < kBkKC / 4; ++k4) {
-                const uint32_t o = km_off(rl, 4 * k4) >> 2;
-                const float4 v = *reinterpret_cast<const float4 *>(tmp + o);
-                uint4 h, l;
-                h.x = to_tf32(v.x); l.x = to_tf32(v.x - __uint_as_float(h.x));
-                h.y = to_tf32(v.y); l.y = to_tf32(v.y - __uint_as_float(h.y));
-                h.z = to_tf32(v.z); l.z = to_tf32(v.z - __uint_as_float(h.z));
-                h.w = to_tf32(v.w); l.w = to_tf32(v.w - __uint_as_float(h.w));
-                *reinterpret_cast<uint4 *>(a_hi + o) = h;
-                *reinterpret_cast<uint4 *>(a_lo + o) = l;
-            }
-        } else {
-            // ---- B: the staged row-major chunk [KC][kBkN] -> the N x K operand
-            const bool landed = mbar_wait_poll(&full[st], (uint32_t)(kc / kBkStages) & 1u, a.err);
-            if (landed) {
-                const float *src = stage + (size_t)st * kBkKC * kBkN;
-                const int i = t - 4 * kWarp;                  // 0..127
-#pragma unroll 8
-                for (int e = i; e < kBkKC * kBkN; e += 4 * kWarp) {
-                    const int k = e / kBkN, n = e % kBkN;
-                    const float v = src[e];
-                    const uint32_t o = km_off(n, k) >> 2;
-                    const uint32_t h = to_tf32(v);
-                    b_hi[o] = h;
-                    b_lo[o] = to_tf32(v - __uint_as_float(h));
-                }
-            }
-            ok = landed;
+    int issued = 0;                                       // chunks the producer requested
+    if (t == 0) {
+        // ---------------------------------------------------------- producer
+        for (int c = 0; c < kBkChunks && ok; ++c) {
+            const int s = c % kBkStages, use = c / kBkStages;
+            if (use > 0) ok = mbar_wait_poll(&done[s], (uint32_t)(use - 1) & 1u, a.err);
+            if (!ok) break;
+            unsigned char *st = stage(s);
+            mbar_arrive_expect_tx(&full[s], kLoadBytes);
+            bulk_g2s(st, apiece + (size_t)c * 2 * kPiece, kPiece, &full[s]);
+            if (HAS_VAL) bulk_g2s(st + kPiece, apiece + (size_t)c * 2 * kPiece + kPiece, kPiece, &full[s]);
+            tensor2d_g2s(st + 2 * kPiece, &bmap, n0, (int)(b0 + c * kBkKC), &full[s]);
+            issued = c + 1;
         }
-        // make the tiles visible to the tensor cores, then one thread issues
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        converted = kc + 1;
-        if (t == 0) {
+    } else if (t == kWarp) {
+        // ------------------------------------------------------- MMA issuer
+        const uint32_t id = instr_desc(kBkM, n_eff);
+        for (int c = 0; c < kBkChunks && ok; ++c) {
+            const int s = c % kBkStages, use = c / kBkStages;
+            ok = mbar_wait_poll(&conv[s], (uint32_t)use & 1u, a.err);
+            if (!ok) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t A_[2] = {smem_addr(a_hi), smem_addr(a_lo)};
-            const uint32_t B_[2] = {smem_addr(b_hi), smem_addr(b_lo)};
+            const uint32_t sa = smem_addr(stage(s));
+            const uint32_t A_[2] = {sa, sa + kPiece};
+            const uint32_t B_[2] = {sa + 2 * kPiece + kBTile, sa + 2 * kPiece + 2 * kBTile};
             const int pa[3] = {0, 0, 1}, pb[3] = {0, 1, 0};
 #pragma unroll
             for (int ps = 0; ps < kPasses; ++ps)
@@ -253,126 +189,249 @@ __global__ void __launch_bounds__(kBkThreads) k_block(const RunArgs a,
                 for (int ks = 0; ks < kBkKC / 8; ++ks)
                     mma_tf32(tmem, smem_desc(A_[pa[ps]] + (uint32_t)ks * 2u * kLBO),
                              smem_desc(B_[pb[ps]] + (uint32_t)ks * 2u * kLBO), id,
-                             (kc | ps | ks) != 0);
+                             (c | ps | ks) != 0);
             asm volatile(
                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                    smem_addr(mma_bar))
+                    smem_addr(&done[s]))
                 : "memory");
         }
-        // stage st has been converted: refill it with chunk kc + kBkStages
-        if (t == tma_thread && kc + kBkStages < kBkChunks) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive_expect_tx(&full[st], kStageBytes);
-            tensor2d_g2s(stage + (size_t)st * kBkKC * kBkN, &bmap, n0,
-                         (int)(b0 + (kc + kBkStages) * kBkKC), &full[st]);
-            ++issued;
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------- off-block entries to shared memory
+        int *orp = reinterpret_cast<int *>(sm + kOffORp);
+        int *ocol = reinterpret_cast<int *>(sm + kOffOCol);
+        float *oval = reinterpret_cast<float *>(sm + kOffOVal);
+        const int i = t - 2 * kWarp;                      // 0..63
+        const int nrows = (int)(a.M - r0 < kBkM ? a.M - r0 : kBkM);
+        const int q0 = a.bk_off_rowptr[r0];
+        for (int k = i; k <= nrows; k += 2 * kWarp) orp[k] = a.bk_off_rowptr[r0 + k] - q0;
+        const int n_off = min(a.bk_off_rowptr[r0 + nrows] - q0, kOffCap);
+        for (int k = i; k < n_off; k += 2 * kWarp) {
+            ocol[k] = __ldg(a.bk_off_col + q0 + k);
+            if (HAS_VAL) oval[k] = __ldg(a.bk_off_val + q0 + k);
         }
-        // the operand tiles are rewritten by the next chunk: wait for the MMAs
-        ok = __syncthreads_and(mbar_wait_poll(mma_bar, (uint32_t)kc & 1u, a.err));
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------- B split
+        const int i = t - 4 * kWarp;                      // 0..127
+        for (int c = 0; c < kBkChunks && ok; ++c) {
+            const int s = c % kBkStages, use = c / kBkStages;
+            ok = mbar_wait_poll(&full[s], (uint32_t)use & 1u, a.err);
+            if (ok && use > 0) ok = mbar_wait_poll(&done[s], (uint32_t)(use - 1) & 1u, a.err);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            unsigned char *st = stage(s);
+            const float *src = reinterpret_cast<const float *>(st + 2 * kPiece);   // [KC][kBkN]
+            uint32_t *bh = reinterpret_cast<uint32_t *>(st + 2 * kPiece + kBTile);
+            uint32_t *bl = reinterpret_cast<uint32_t *>(st + 2 * kPiece + 2 * kBTile);
+            // thread i owns column n = i: four k at a time into one 16-byte
+            // word of the K-major tile (a quarter-warp stores 128 contiguous bytes)
+#pragma unroll
+            for (int k4 = 0; k4 < kBkKC / 4; ++k4) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const float v = src[(4 * k4 + kk) * kBkN + i];
+                    h[kk] = to_tf32(v);
+                    l[kk] = to_tf32(v - __uint_as_float(h[kk]));
+                }
+                const uint32_t o = km_off(i, 4 * k4) >> 2;
+                *reinterpret_cast<uint4 *>(bh + o) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(bl + o) = make_uint4(l[0], l[1], l[2], l[3]);
+            }
+            // the split tiles are read by the tensor cores (async proxy)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&conv[s]);
+        }
     }
-    // never leave while a tensor copy may still be landing in this CTA's memory
-    // (only after an early exit are requested chunks left unconverted)
-    if (t == tma_thread)
-        for (int kc = converted; kc < issued; ++kc)
-            mbar_wait_poll(&full[kc % kBkStages], (uint32_t)(kc / kBkStages) & 1u, a.err);
-    const int qb = q + cons;              // first entry past the block (sorted rows, A side)
+    // the accumulator is complete once the last chunk's MMAs have read their
+    // stage (a commit tracks every earlier MMA of the issuing thread)
+    ok = __syncthreads_and(ok);
+    if (ok) ok = mbar_wait_poll(&done[(kBkChunks - 1) % kBkStages],
+                                (uint32_t)((kBkChunks - 1) / kBkStages) & 1u, a.err);
+    ok = __syncthreads_and(ok);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
     if (ok) {
-        // The accumulator goes through shared memory (the operand and staging
-        // tiles are free now) so that rows can be finished warp-cooperatively:
-        // lanes across columns, one coalesced B-row read per entry outside the
-        // diagonal block. Per element the order stays: the block's dense sum,
-        // then the other entries in CSR order.
-        __shared__ int s_qa[kBkM], s_qb[kBkM];
-        if (a_side) {
-            s_qa[rl] = qa;
-            s_qb[rl] = qb;
-        }
-        float *tile = reinterpret_cast<float *>(sm);       // [kBkM][kTilePitch]
+        // The accumulator goes through shared memory (the stages are free now)
+        // so that rows are finished warp-cooperatively: lanes across columns,
+        // one coalesced B-row read per entry outside the diagonal block. Per
+        // element the order is the block's dense sum, then the other entries
+        // in CSR order.
+        float *tile_s = reinterpret_cast<float *>(sm);      // [kBkM][kTilePitch]
+        const int rl = (warp & 3) * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         for (int c = (warp >> 2) * 16; c < n_eff; c += 32) {
             float v[16];
             tmem_ld16(trow + (uint32_t)c, v);
-            float4 *dst = reinterpret_cast<float4 *>(tile + rl * kTilePitch + c);
+            float4 *dst = reinterpret_cast<float4 *>(tile_s + rl * kTilePitch + c);
 #pragma unroll
             for (int e4 = 0; e4 < 4; ++e4)
                 dst[e4] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
         }
         __syncthreads();
+        // Rows are finished four at a time per warp (rows rr0 + 8 k), up to
+        // kEB entries of each in one step: twelve gathers in flight per lane
+        // (the register budget of two CTAs per SM).
+        // The entries come from the staged copy (the first kOffCap of the
+        // CTA), else from global memory.
+        const int *orp = reinterpret_cast<const int *>(sm + kOffORp);
+        const int *ocol = reinterpret_cast<const int *>(sm + kOffOCol);
+        const float *oval = reinterpret_cast<const float *>(sm + kOffOVal);
+        const int q0g = a.bk_off_rowptr[r0];
         const int cl = 4 * lane;                            // this lane's 4 columns
         const bool col_ok = cl < n_eff;
         const int cc = col_ok ? cl : 0;
-        for (int rr = warp; rr < kBkM; rr += kBkThreads / kWarp) {
-            const int64_t i = r0 + rr;
-            if (i >= a.M) break;
-            const int e0 = a.rowptr[i], e1 = a.rowptr[i + 1];
-            float4 acc = *reinterpret_cast<const float4 *>(tile + rr * kTilePitch + cc);
-            const float *Bc = a.B + n0 + cc;
-            auto add4 = [&](int pb, int pe) {               // entries [pb, pe), 4 in flight
-                int p = pb;
-                for (; p + 4 <= pe; p += 4) {
-                    int j[4];
-                    float w[4];
-                    float4 x[4];
+        const float *Bc = a.B + n0 + cc;
+        const int nrows = (int)(a.M - r0 < kBkM ? a.M - r0 : kBkM);
+        constexpr int kRB = 4;                              // rows per batch
+        constexpr int kEB = 3;                              // entries per row per step
+        for (int rr0 = warp; rr0 < nrows; rr0 += kRB * (kBkThreads / kWarp)) {
+            int qa[kRB], qb[kRB];
+            float4 acc[kRB];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        j[u] = __ldg(a.col + p + u);
-                        w[u] = HAS_VAL ? __ldg(a.val + p + u) : 1.0f;
+            for (int k = 0; k < kRB; ++k) {
+                const int rr = rr0 + k * (kBkThreads / kWarp);
+                const bool live = rr < nrows;
+                qa[k] = live ? orp[rr] : 0;
+                qb[k] = live ? orp[rr + 1] : 0;
+                acc[k] = live ? *reinterpret_cast<const float4 *>(tile_s + rr * kTilePitch + cc)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            bool more = true;
+            while (more) {                                  // uniform across the warp
+                int j[kRB][kEB];
+                float w[kRB][kEB];
+                float4 x[kRB][kEB];
+#pragma unroll
+                for (int k = 0; k < kRB; ++k)
+#pragma unroll
+                    for (int u = 0; u < kEB; ++u) {
+                        const int q = qa[k] + u;
+                        const bool in = q < qb[k];
+                        j[k][u] = !in ? 0 : q < kOffCap ? ocol[q] : __ldg(a.bk_off_col + q0g + q);
+                        w[k][u] = (!HAS_VAL || !in) ? 1.0f
+                                  : q < kOffCap ? oval[q] : __ldg(a.bk_off_val + q0g + q);
                     }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) x[u] = __ldg(reinterpret_cast<const float4 *>(Bc + (int64_t)j[u] * N));
+                for (int k = 0; k < kRB; ++k)
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        acc.x = __fmaf_rn(w[u], x[u].x, acc.x);
-                        acc.y = __fmaf_rn(w[u], x[u].y, acc.y);
-                        acc.z = __fmaf_rn(w[u], x[u].z, acc.z);
-                        acc.w = __fmaf_rn(w[u], x[u].w, acc.w);
-                    }
-                }
-                for (; p < pe; ++p) {
-                    const int j = __ldg(a.col + p);
-                    const float w = HAS_VAL ? __ldg(a.val + p) : 1.0f;
-                    const float4 x = __ldg(reinterpret_cast<const float4 *>(Bc + (int64_t)j * N));
-                    acc.x = __fmaf_rn(w, x.x, acc.x);
-                    acc.y = __fmaf_rn(w, x.y, acc.y);
-                    acc.z = __fmaf_rn(w, x.z, acc.z);
-                    acc.w = __fmaf_rn(w, x.w, acc.w);
-                }
-            };
-            if (a.rows_sorted) {
-                add4(e0, s_qa[rr]);
-                add4(s_qb[rr], e1);
-            } else {
-                for (int p = e0; p < e1; ++p) {
-                    const int j = __ldg(a.col + p);
-                    if ((uint64_t)((int64_t)j - b0) < (uint64_t)kBlockRows) continue;
-                    const float w = HAS_VAL ? __ldg(a.val + p) : 1.0f;
-                    const float4 x = __ldg(reinterpret_cast<const float4 *>(Bc + (int64_t)j * N));
-                    acc.x = __fmaf_rn(w, x.x, acc.x);
-                    acc.y = __fmaf_rn(w, x.y, acc.y);
-                    acc.z = __fmaf_rn(w, x.z, acc.z);
-                    acc.w = __fmaf_rn(w, x.w, acc.w);
+                    for (int u = 0; u < kEB; ++u)
+                        if (qa[k] + u < qb[k])
+                            x[k][u] = __ldg(reinterpret_cast<const float4 *>(Bc + (int64_t)j[k][u] * N));
+                more = false;
+#pragma unroll
+                for (int k = 0; k < kRB; ++k) {
+#pragma unroll
+                    for (int u = 0; u < kEB; ++u)
+                        if (qa[k] + u < qb[k]) {
+                            acc[k].x = __fmaf_rn(w[k][u], x[k][u].x, acc[k].x);
+                            acc[k].y = __fmaf_rn(w[k][u], x[k][u].y, acc[k].y);
+                            acc[k].z = __fmaf_rn(w[k][u], x[k][u].z, acc[k].z);
+                            acc[k].w = __fmaf_rn(w[k][u], x[k][u].w, acc[k].w);
+                        }
+                    qa[k] += kEB;
+                    more |= qa[k] < qb[k];
                 }
             }
-            float out[4] = {acc.x, acc.y, acc.z, acc.w};
-            if (RED == SPMM_MEAN) {
-                const int d = e1 - e0;
-                const float inv_d = d > 0 ? rcp_approx((float)d) : 0.0f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) out[e] = __fmul_rn(out[e], inv_d);
-            }
-            if (col_ok) {
-                epilogue<4>(a, (int64_t)n0 + cl, out);
-                st_vec<4>(a.C + i * N + n0 + cl, out);
+            for (int k = 0; k < kRB; ++k) {
+                const int rr = rr0 + k * (kBkThreads / kWarp);
+                if (rr >= nrows) break;
+                const int64_t i = r0 + rr;
+                float out[4] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w};
+                if (RED == SPMM_MEAN) {
+                    const int d = a.rowptr[i + 1] - a.rowptr[i];
+                    const float inv_d = d > 0 ? rcp_approx((float)d) : 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) out[e] = __fmul_rn(out[e], inv_d);
+                }
+                if (col_ok) {
+                    epilogue<4>(a, (int64_t)n0 + cl, out);
+                    st_vec<4>(a.C + i * N + n0 + cl, out);
+                }
             }
         }
+    } else if (t == 0) {
+        // never leave while a copy this CTA requested may still be landing:
+        // wait (bounded) for the last request of each stage
+        for (int c = max(0, issued - kBkStages); c < issued; ++c)
+            mbar_wait_poll(&full[c % kBkStages], (uint32_t)(c / kBkStages) & 1u, a.err);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBkN)
                      : "memory");
+}
+
+// ------------------------------------------------------------- preparation
+// Densify: one thread per row adds its entries inside the diagonal block into
+// the row tile's hi pieces (fp32, CSR order); the pieces start zeroed.
+__global__ void k_bk_densify(const int32_t *__restrict__ rowptr, const int32_t *__restrict__ col,
+                             const float *__restrict__ val, int64_t M, int64_t K,
+                             unsigned char *__restrict__ tiles) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= M) return;
+    const int64_t tile = i / kBkM, b0 = i / kBlockRows * kBlockRows;
+    const int r = (int)(i % kBkM);
+    unsigned char *base = tiles + (size_t)tile * kTileBytes;
+    for (int p = rowptr[i]; p < rowptr[i + 1]; ++p) {
+        const int64_t c = col[p];
+        if (c < b0 || c >= b0 + kBlockRows || c >= K) continue;
+        const int k = (int)(c - b0), chunk = k / kBkKC;
+        float *hi = reinterpret_cast<float *>(base + (size_t)chunk * 2 * kPiece);
+        hi[km_off(r, k % kBkKC) >> 2] += val ? val[p] : 1.0f;
+    }
+}
+
+// Split every fp32 sum of the hi pieces into TF32 hi and lo (lo = 0 when A is
+// unweighted: its sums are small integers, exact in TF32).
+__global__ void k_bk_split(unsigned char *__restrict__ tiles, int64_t n_pieces) {
+    constexpr int kWords = (int)(kPiece / 4);
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n_pieces * kWords;
+         q += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t piece = q / kWords, w = q % kWords;
+        uint32_t *hi = reinterpret_cast<uint32_t *>(tiles + (size_t)piece * 2 * kPiece);
+        uint32_t *lo = hi + kWords;
+        const float x = __uint_as_float(hi[w]);
+        const uint32_t h = to_tf32(x);
+        hi[w] = h;
+        lo[w] = to_tf32(x - __uint_as_float(h));
+    }
+}
+
+// The entries outside the diagonal block: per-row counts, then (at the
+// scanned offsets) the entries themselves in CSR order.
+__global__ void k_bk_off_count(const int32_t *__restrict__ rowptr, const int32_t *__restrict__ col,
+                               int64_t M, int32_t *__restrict__ cnt) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= M) return;
+    const int64_t b0 = i / kBlockRows * kBlockRows;
+    int n = 0;
+    for (int p = rowptr[i]; p < rowptr[i + 1]; ++p) {
+        const int64_t c = col[p];
+        n += (c < b0 || c >= b0 + kBlockRows);
+    }
+    cnt[i] = n;
+}
+
+__global__ void k_bk_off_fill(const int32_t *__restrict__ rowptr, const int32_t *__restrict__ col,
+                              const float *__restrict__ val, int64_t M,
+                              const int32_t *__restrict__ off_rowptr, int32_t *__restrict__ off_col,
+                              float *__restrict__ off_val) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= M) return;
+    const int64_t b0 = i / kBlockRows * kBlockRows;
+    int q = off_rowptr[i];
+    for (int p = rowptr[i]; p < rowptr[i + 1]; ++p) {
+        const int64_t c = col[p];
+        if (c >= b0 && c < b0 + kBlockRows) continue;
+        off_col[q] = (int32_t)c;
+        if (off_val) off_val[q] = val[p];
+        ++q;
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -408,16 +467,96 @@ cudaError_t go(const RunArgs &a, cudaStream_t s) {
     auto kern = k_block<RED, HAS_VAL>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBkSmem);
     if (e != cudaSuccess) return e;
-    const unsigned gx = (unsigned)((a.M + kBkM - 1) / kBkM);
-    const unsigned gy = (unsigned)((a.N + kBkN - 1) / kBkN);
+    const unsigned gx = (unsigned)((a.N + kBkN - 1) / kBkN);
+    const unsigned gy = (unsigned)((a.M + kBkM - 1) / kBkM);
     kern<<<dim3(gx, gy), kBkThreads, kBkSmem, s>>>(a, map);
     count_launch();
     return cudaGetLastError();
 }
 
+void free_prepared(Plan *p) {
+    if (p->bk_tiles) cudaFree(p->bk_tiles);
+    if (p->bk_off_rowptr) cudaFree(p->bk_off_rowptr);
+    if (p->bk_off_col) cudaFree(p->bk_off_col);
+    if (p->bk_off_val) cudaFree(p->bk_off_val);
+    p->bk_tiles = nullptr;
+    p->bk_off_rowptr = nullptr;
+    p->bk_off_col = nullptr;
+    p->bk_off_val = nullptr;
+    p->bk_flavor = -1;
+    p->bk_bytes = 0;
+    p->bk_n_off = 0;
+}
+
 }  // namespace
 
-// Requires N % 16 == 0, 16-byte aligned B and C, reduce SUM or MEAN.
+void block_free(Plan *p) { free_prepared(p); }
+
+size_t block_prepared_bytes(int64_t M, int64_t n_off, bool has_val) {
+    const int64_t tiles = (M + kBkM - 1) / kBkM;
+    return (size_t)tiles * kTileBytes + 4 * (size_t)(M + 1) + (has_val ? 8 : 4) * (size_t)n_off;
+}
+
+cudaError_t block_prepare(Plan *p, const int32_t *col, const float *val, cudaStream_t s) {
+    free_prepared(p);
+    const int64_t M = p->M;
+    if (M == 0) return cudaSuccess;
+    const int64_t tiles = (M + kBkM - 1) / kBkM;
+    const size_t tbytes = (size_t)tiles * kTileBytes;
+    const unsigned grid = (unsigned)((M + 255) / 256);
+    cudaError_t e = cudaMalloc(&p->bk_tiles, tbytes);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&p->bk_off_rowptr, sizeof(int32_t) * (M + 1));
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->bk_tiles, 0, tbytes, s);
+    if (e == cudaSuccess) {
+        k_bk_densify<<<grid, 256, 0, s>>>(p->rowptr, col, val, M, p->K,
+                                          reinterpret_cast<unsigned char *>(p->bk_tiles));
+        k_bk_split<<<(unsigned)std::min<int64_t>(tiles * kBkChunks * 8, 65535), 256, 0, s>>>(
+            reinterpret_cast<unsigned char *>(p->bk_tiles), tiles * kBkChunks);
+        k_bk_off_count<<<grid, 256, 0, s>>>(p->rowptr, col, M, p->bk_off_rowptr);
+        count_launch(3);
+        e = cudaGetLastError();
+    }
+    // exclusive scan of the counts on the host (plan time)
+    std::vector<int32_t> cnt((size_t)M + 1, 0);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(cnt.data(), p->bk_off_rowptr, sizeof(int32_t) * M,
+                            cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        free_prepared(p);
+        return e;
+    }
+    int64_t run = 0;
+    for (int64_t i = 0; i < M; ++i) {
+        const int32_t c = cnt[i];
+        cnt[i] = (int32_t)run;
+        run += c;
+    }
+    cnt[M] = (int32_t)run;
+    p->bk_n_off = run;
+    e = cudaMemcpyAsync(p->bk_off_rowptr, cnt.data(), sizeof(int32_t) * (M + 1),
+                        cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&p->bk_off_col, sizeof(int32_t) * std::max<int64_t>(1, run));
+    if (e == cudaSuccess && val)
+        e = cudaMalloc((void **)&p->bk_off_val, sizeof(float) * std::max<int64_t>(1, run));
+    if (e == cudaSuccess) {
+        k_bk_off_fill<<<grid, 256, 0, s>>>(p->rowptr, col, val, M, p->bk_off_rowptr,
+                                           p->bk_off_col, p->bk_off_val);
+        count_launch();
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        free_prepared(p);
+        return e;
+    }
+    p->bk_flavor = val ? 1 : 0;
+    p->bk_bytes = (int64_t)block_prepared_bytes(M, run, val != nullptr);
+    return cudaSuccess;
+}
+
+// Requires N % 16 == 0, 16-byte aligned B and C, reduce SUM or MEAN, and the
+// plan's prepared blocks (a.bk_*) for this flavour of A.
 cudaError_t launch_block(const RunArgs &a, int reduce, bool has_val, cudaStream_t s) {
     if (reduce == SPMM_SUM) return has_val ? go<SPMM_SUM, true>(a, s) : go<SPMM_SUM, false>(a, s);
     if (reduce == SPMM_MEAN) return has_val ? go<SPMM_MEAN, true>(a, s) : go<SPMM_MEAN, false>(a, s);

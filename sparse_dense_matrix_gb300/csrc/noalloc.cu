@@ -26,8 +26,10 @@ constexpr int kNaMaxChunks = 1 << 18;                       // chunks per call
 constexpr int kNaMaxDevices = 64;
 
 // layout of the array (bytes)
+constexpr int kNaMaxBlocks = 1 << 16;                               // row blocks per call
 constexpr size_t kNaOffHeader = 0;                                   // int32 [16]
-constexpr size_t kNaOffRows = 256;                                   // int32 [kNaMaxHeavy]
+constexpr size_t kNaOffBlocks = 256;                                 // int4 [kNaMaxBlocks]
+constexpr size_t kNaOffRows = kNaOffBlocks + 16 * size_t(kNaMaxBlocks); // int32 [kNaMaxHeavy]
 constexpr size_t kNaOffChunk0 = kNaOffRows + 4 * size_t(kNaMaxHeavy);  // int32 [kNaMaxHeavy + 1]
 constexpr size_t kNaOffChunks =
     (kNaOffChunk0 + 4 * size_t(kNaMaxHeavy + 1) + 255) / 256 * 256;   // int2 [kNaMaxChunks]
@@ -39,75 +41,139 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kStaticScratchB
 
 namespace {
 
-// One CTA walks all rows in rounds of 1024: rows above t_split are listed in
-// row order with the index of their first chunk (ceil(d / chunk) chunks each).
-// Header: [0] split rows, [1] chunks, [2] table overflow, [3] decreasing rowptr.
-__global__ void __launch_bounds__(1024) k_na_build(const int32_t *__restrict__ rowptr, int64_t M,
-                                                   int t_split, int chunk,
-                                                   int32_t *__restrict__ hdr,
-                                                   int32_t *__restrict__ rows,
-                                                   int32_t *__restrict__ chunk0) {
-    __shared__ int s_cnt[32], s_q[32];
-    __shared__ int s_base, s_cbase, s_bad;
+constexpr int kNaThreads = 256;
+
+// The split rows (above t_split) and their chunk counts, in three passes over
+// row blocks of `rpb` rows: (1) per block, the split rows, their chunks and
+// any decreasing row pointer; (2) one CTA turns the counts into each block's
+// first list position and first chunk (exclusive scans, in block order) and
+// writes the header: [0] split rows, [1] chunks, [2] table overflow,
+// [3] decreasing rowptr; (3) per block, its split rows in row order with the
+// index of their first chunk (ceil(d / chunk) chunks each).
+__device__ __forceinline__ int na_chunks(int d, int t_split, int chunk) {
+    return d > t_split ? (d + chunk - 1) / chunk : 0;
+}
+
+__global__ void __launch_bounds__(kNaThreads) k_na_count(const int32_t *__restrict__ rowptr,
+                                                         int64_t M, int64_t rpb, int t_split,
+                                                         int chunk, int4 *__restrict__ blocks) {
+    const int64_t r0 = (int64_t)blockIdx.x * rpb, r1 = min(M, r0 + rpb);
+    int heavy = 0, chunks = 0, bad = 0;
+    for (int64_t r = r0 + threadIdx.x; r < r1; r += kNaThreads) {
+        const int d = rowptr[r + 1] - rowptr[r];
+        bad |= d < 0;
+        heavy += d > t_split;
+        chunks += na_chunks(d, t_split, chunk);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        heavy += __shfl_xor_sync(0xffffffffu, heavy, o);
+        chunks += __shfl_xor_sync(0xffffffffu, chunks, o);
+    }
+    bad = __syncthreads_or(bad);
+    __shared__ int sh[2][kNaThreads / 32];
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        sh[0][w] = heavy;
+        sh[1][w] = chunks;
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
-        s_base = 0;
-        s_cbase = 0;
+        int h = 0, c = 0;
+        for (int i = 0; i < kNaThreads / 32; ++i) {
+            h += sh[0][i];
+            c += sh[1][i];
+        }
+        blocks[blockIdx.x] = make_int4(h, c, bad, 0);
+    }
+}
+
+__global__ void __launch_bounds__(1024) k_na_scan(int4 *__restrict__ blocks, int64_t nblk,
+                                                  int32_t *__restrict__ hdr) {
+    __shared__ int s_h[32], s_c[32];
+    __shared__ int s_bh, s_bc, s_bad;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        s_bh = 0;
+        s_bc = 0;
         s_bad = 0;
     }
     __syncthreads();
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (int64_t r0 = 0; r0 < M; r0 += 1024) {
-        const int64_t r = r0 + threadIdx.x;
-        int d = 0;
-        if (r < M) {
-            d = rowptr[r + 1] - rowptr[r];
-            if (d < 0) atomicOr(&s_bad, 1);
+    for (int64_t base = 0; base < nblk; base += 1024) {
+        const int64_t b = base + threadIdx.x;
+        int4 v = b < nblk ? blocks[b] : make_int4(0, 0, 0, 0);
+        int h = v.x, c = v.y;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {       // inclusive warp scans
+            const int th = __shfl_up_sync(0xffffffffu, h, o), tc = __shfl_up_sync(0xffffffffu, c, o);
+            if (lane >= o) { h += th; c += tc; }
         }
+        if (lane == 31) { s_h[w] = h; s_c[w] = c; }
+        if (v.z) atomicOr(&s_bad, 1);
+        __syncthreads();
+        int hb = s_bh, cb = s_bc, ht = 0, ct = 0;
+        for (int i = 0; i < 32; ++i) {
+            if (i < w) { hb += s_h[i]; cb += s_c[i]; }
+            ht += s_h[i];
+            ct += s_c[i];
+        }
+        if (b < nblk) blocks[b] = make_int4(hb + h - v.x, cb + c - v.y, v.z, 0);
+        __syncthreads();
+        if (threadIdx.x == 0) { s_bh += ht; s_bc += ct; }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        hdr[0] = s_bh;
+        hdr[1] = s_bc;
+        hdr[2] = (s_bh > kNaMaxHeavy || s_bc > kNaMaxChunks) ? 1 : 0;
+        hdr[3] = s_bad;
+    }
+}
+
+__global__ void __launch_bounds__(kNaThreads) k_na_list(const int32_t *__restrict__ rowptr,
+                                                        int64_t M, int64_t rpb, int t_split,
+                                                        int chunk, const int4 *__restrict__ blocks,
+                                                        const int32_t *__restrict__ hdr,
+                                                        int32_t *__restrict__ rows,
+                                                        int32_t *__restrict__ chunk0) {
+    __shared__ int s_cnt[kNaThreads / 32], s_q[kNaThreads / 32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t r0 = (int64_t)blockIdx.x * rpb, r1 = min(M, r0 + rpb);
+    const int4 off = blocks[blockIdx.x];
+    int base = off.x, cbase = off.y;
+    for (int64_t rb = r0; rb < r1; rb += kNaThreads) {
+        const int64_t r = rb + threadIdx.x;
+        const int d = r < r1 ? rowptr[r + 1] - rowptr[r] : 0;
         const bool heavy = d > t_split;
-        const int q = heavy ? (d + chunk - 1) / chunk : 0;
+        const int q = na_chunks(d, t_split, chunk);
         const unsigned m = __ballot_sync(0xffffffffu, heavy);
-        const int rank = __popc(m & ((1u << lane) - 1u));
-        int qs = q;   // inclusive scan of chunk counts within the warp
+        int qs = q;                               // inclusive scan of chunk counts in the warp
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, qs, o);
-            if (lane >= o) qs += t;
+            const int tq = __shfl_up_sync(0xffffffffu, qs, o);
+            if (lane >= o) qs += tq;
         }
-        if (lane == 31) {
-            s_cnt[w] = __popc(m);
-            s_q[w] = qs;
-        }
+        if (lane == 31) { s_cnt[w] = __popc(m); s_q[w] = qs; }
         __syncthreads();
         int before = 0, qbefore = 0, tot = 0, qtot = 0;
-        for (int i = 0; i < 32; ++i) {
-            if (i < w) {
-                before += s_cnt[i];
-                qbefore += s_q[i];
-            }
+        for (int i = 0; i < kNaThreads / 32; ++i) {
+            if (i < w) { before += s_cnt[i]; qbefore += s_q[i]; }
             tot += s_cnt[i];
             qtot += s_q[i];
         }
         if (heavy) {
-            const int pos = s_base + before + rank;
+            const int pos = base + before + __popc(m & ((1u << lane) - 1u));
             if (pos < kNaMaxHeavy) {
                 rows[pos] = (int32_t)r;
-                chunk0[pos] = s_cbase + qbefore + qs - q;
+                chunk0[pos] = cbase + qbefore + qs - q;
             }
         }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            s_base += tot;
-            s_cbase += qtot;
-        }
+        base += tot;
+        cbase += qtot;
         __syncthreads();
     }
-    if (threadIdx.x == 0) {
-        hdr[0] = s_base;
-        hdr[1] = s_cbase;
-        hdr[2] = (s_base > kNaMaxHeavy || s_cbase > kNaMaxChunks) ? 1 : 0;
-        hdr[3] = s_bad;
-        if (s_base <= kNaMaxHeavy) chunk0[s_base] = s_cbase;
-    }
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0 && hdr[0] <= kNaMaxHeavy)
+        chunk0[hdr[0]] = hdr[1];
 }
 
 // One warp per split row writes the (row, first entry) pair of each chunk.
@@ -196,8 +262,15 @@ extern "C" spmm_status spmm_run_noalloc(const int32_t *rowptr, const int32_t *co
     // split rows and their chunk table, counted on the device and read back
     const int64_t t_split = spmm_default_t_split(M, nnz, num_sms);
     const int64_t chunk = std::max<int64_t>(32, t_split / 2);
-    k_na_build<<<1, 1024, 0, s>>>(rowptr, M, (int)t_split, (int)chunk, hdr, rows, chunk0);
-    count_launch();
+    const int64_t rpb = std::max<int64_t>(4096, (M + kNaMaxBlocks - 1) / kNaMaxBlocks);
+    const int64_t nblk = (M + rpb - 1) / rpb;
+    int4 *blocks = reinterpret_cast<int4 *>(scratch + kNaOffBlocks);
+    k_na_count<<<(unsigned)nblk, kNaThreads, 0, s>>>(rowptr, M, rpb, (int)t_split, (int)chunk,
+                                                     blocks);
+    k_na_scan<<<1, 1024, 0, s>>>(blocks, nblk, hdr);
+    k_na_list<<<(unsigned)nblk, kNaThreads, 0, s>>>(rowptr, M, rpb, (int)t_split, (int)chunk,
+                                                    blocks, hdr, rows, chunk0);
+    count_launch(3);
     int32_t h[4] = {0, 0, 0, 0};
     e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaMemcpyAsync(h, hdr, sizeof(h), cudaMemcpyDeviceToHost, s);

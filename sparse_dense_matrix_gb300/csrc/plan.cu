@@ -233,6 +233,26 @@ __global__ void __launch_bounds__(256) k_check_cols(const int32_t *__restrict__ 
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err + kErrBadCol, 1);
 }
 
+// SEGMENT tiles: tile t starts at merge-path item k = t * kSegItems (items are
+// the row ends and the stored entries, a row's end after its entries). After k
+// items the path has passed r row ends, r the largest row index with
+// rowptr[r] + r <= k (rowptr[r] + r strictly increases with r), and
+// e = k - r entries. One thread per tile boundary, a binary search each.
+__global__ void k_seg_tiles(const int32_t *__restrict__ rowptr, int64_t M, int64_t items,
+                            int64_t n_tiles, int2 *__restrict__ out) {
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t <= n_tiles;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t k = min(t * (int64_t)kSegItems, items);
+        int64_t lo = 0, hi = M;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            if ((int64_t)rowptr[mid] + mid <= k) lo = mid;
+            else hi = mid - 1;
+        }
+        out[t] = make_int2((int)lo, (int)(k - lo));
+    }
+}
+
 // ------------------------------------------------------------- host helpers
 int64_t pow2ceil(int64_t x) {
     int64_t p = 1;
@@ -344,10 +364,28 @@ done:
 void destroy(Plan *p) {
     if (!p) return;
     free_heavy(p);
+    block_free(p);
+    dev_free(p->seg_tiles);
     dev_free(p->rowptr);
     dev_free(p->work);
     dev_free(p->err);
     delete p;
+}
+
+// The SEGMENT family's tile table (see k_seg_tiles).
+spmm_status seg_build(Plan *p, cudaStream_t s) {
+    const int64_t items = p->M + p->nnz;
+    p->seg_n_tiles = (items + kSegItems - 1) / kSegItems;
+    cudaError_t e = dev_alloc((void **)&p->seg_tiles, sizeof(int2) * (p->seg_n_tiles + 1));
+    if (e != cudaSuccess) return from_cuda(e);
+    const int64_t blocks = std::min<int64_t>((p->seg_n_tiles + 256) / 256, 4096);
+    k_seg_tiles<<<(unsigned)std::max<int64_t>(1, blocks), 256, 0, s>>>(p->rowptr, p->M, items,
+                                                                       p->seg_n_tiles,
+                                                                       p->seg_tiles);
+    count_launch();
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return from_cuda(e);
 }
 
 size_t workspace_need(const Plan *p, int64_t N, int reduce) {
@@ -388,9 +426,11 @@ spmm_status plan_ensure_workspace(Plan *p, size_t need) { return ensure_workspac
 //   R1a BLOCK (tensor cores) only when pinned;
 //   R2  wide N (more than 32 column vectors per row)        -> WARPROW with column
 //       tiles (COLTILE, the staged variant, measured 1.1-1.7x slower: pin only);
-//   R3  near-uniform degrees (CV_d <= 1) and narrow N (L < 32 lanes, so
+//   R3  skewed degrees (CV_d > 1), N <= 16 in 128-bit vectors, col/val
+//       16-byte aligned                                       -> SEGMENT (merge-path tiles);
+//   R4  near-uniform degrees (CV_d <= 1) and narrow N (L < 32 lanes, so
 //       several rows share a warp)                            -> ROWGROUP, 32/L rows per warp;
-//   R4  otherwise (skewed degrees)                            -> WARPROW.
+//   R5  otherwise (skewed degrees)                            -> WARPROW.
 // Independently of the family, rows with more than t_split entries are split
 // into chunks (two extra launches) whenever the plan holds such rows.
 // `aligned`: bit 0 = B/C/argmax 16-byte aligned, bit 1 = col/val 16-byte aligned,
@@ -464,14 +504,26 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     }
     // COLTILE needs 128-bit vectors (N % 4 == 0, aligned B/C); else WARPROW tiles
     const bool coltile_ok = o->vec == 4;
+    // SEGMENT needs 128-bit vectors and col/val that bulk copies may read
+    // (16-byte aligned)
+    const bool segment_ok = o->vec == 4 && (aligned & 2) && d->M > 0 && d->seg_tiles > 0;
     if (fam == -2) {
         if (family_override == SPMM_FAMILY_COLTILE)
             fam = coltile_ok ? SPMM_FAMILY_COLTILE : SPMM_FAMILY_WARPROW;
+        else if (family_override == SPMM_FAMILY_SEGMENT)
+            fam = segment_ok ? SPMM_FAMILY_SEGMENT : SPMM_FAMILY_WARPROW;
         else if (family_override != SPMM_FAMILY_AUTO && family_override != SPMM_FAMILY_WINDOW &&
                  family_override != SPMM_FAMILY_BLOCK)
             fam = family_override;
         else if (n_vec > 32)
             fam = SPMM_FAMILY_WARPROW;   // measured faster than COLTILE on the wide workloads
+        else if (segment_ok && d->cv > 1.0 && n_vec <= 4)
+            // skewed degrees at narrow N (four lanes or fewer per entry): the
+            // merge-path tiles keep every lane's gathers in flight where a warp
+            // per row waits on short rows (Chung-Lu 4M, N=16: 1.37 against
+            // 1.71 ms for the sum, 1.81 against 2.24 ms for max); at N=64 and
+            // wider WARPROW measured 8-40% faster
+            fam = SPMM_FAMILY_SEGMENT;
         else if (d->cv <= 1.0 && lanes < 32)
             // a 32-lane ROWGROUP holds one row per warp like WARPROW, without
             // WARPROW's batched loads (community graph, N=128: 104 against 94 us)
@@ -480,13 +532,28 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
             fam = SPMM_FAMILY_WARPROW;
     }
     if (fam == SPMM_FAMILY_COLTILE) lanes = 32;     // one 128-column tile per warp
+    // SEGMENT: L lanes x Q four-column chunks per lane; two chunks when a row
+    // is wider than 128 columns, column tiles of 256 beyond that
+    const int64_t seg_q = n_vec > 32 ? 2 : 1;
     o->lanes = (int32_t)lanes;
     if (fam == SPMM_FAMILY_BLOCK) lanes = 32;
-    o->col_tiles = fam == SPMM_FAMILY_WINDOW  ? (int32_t)win_tiles
-                   : fam == SPMM_FAMILY_BLOCK ? (int32_t)((N + 127) / 128)
-                                              : (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
+    o->col_tiles = fam == SPMM_FAMILY_WINDOW    ? (int32_t)win_tiles
+                   : fam == SPMM_FAMILY_BLOCK   ? (int32_t)((N + 127) / 128)
+                   : fam == SPMM_FAMILY_SEGMENT ? (int32_t)((n_vec + lanes * seg_q - 1) / (lanes * seg_q))
+                                                : (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
     o->family = fam;
     o->rows_per_warp = fam == SPMM_FAMILY_ROWGROUP ? (int32_t)(32 / lanes) : 1;
+    o->seg_warps = 0;
+    o->seg_chunks = 0;
+    if (fam == SPMM_FAMILY_SEGMENT) {
+        // every row, however long, goes through the merge-path tiles: no split
+        o->seg_chunks = (int32_t)seg_q;
+        o->seg_warps = (int32_t)segment_warps(d->seg_tiles, num_sms, o->col_tiles);
+        o->launches = (d->M > 0 && N > 0) ? 2 : 0;
+        o->workspace_bytes = (int64_t)segment_workspace(o->seg_warps, o->col_tiles, (int)lanes,
+                                                        (int)seg_q, reduce);
+        return;
+    }
     const bool split = d->n_heavy > 0 && fam != SPMM_FAMILY_BLOCK;
     o->launches = (d->M > 0 && N > 0) ? 1 + (split ? 2 : 0) : 0;
     const size_t per = (size_t)d->n_chunks * (size_t)N * 4;
@@ -515,7 +582,7 @@ spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce
                        int num_sms, int family_override, spmm_plan_info *out) {
     if (!desc || !out || N < 0) return SPMM_ERR_INVALID_ARG;
     if (reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
-    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_BLOCK)
+    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_SEGMENT)
         return SPMM_ERR_INVALID_ARG;
     route_fill(desc, N, reduce, aligned, num_sms, family_override, out);
     return SPMM_OK;
@@ -589,6 +656,7 @@ static spmm_status create_plan(const int32_t *rowptr, int64_t row_begin, int64_t
         }
         p->t_split_default = spmm_default_t_split(M, p->nnz, p->num_sms);
         st = analyse(p, p->t_split_default, s);
+        if (st == SPMM_OK && M > 0) st = seg_build(p, s);
     }
     t_alloc_countdown = 0;
     if (st != SPMM_OK) {
@@ -669,6 +737,8 @@ static void fill_desc(const Plan *p, spmm_plan_info *o) {
     o->blk_intra = p->blk_intra;
     o->band_cover = p->band_cover;
     o->row0 = p->row0;
+    o->seg_tiles = p->seg_n_tiles;
+    o->block_bytes = p->bk_bytes;
 }
 
 spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce, spmm_plan_info *out) {
@@ -680,7 +750,7 @@ spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce, 
 }
 
 spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split) {
-    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_BLOCK) return SPMM_ERR_INVALID_ARG;
+    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_SEGMENT) return SPMM_ERR_INVALID_ARG;
     Plan *p = reinterpret_cast<Plan *>(plan);
     p->family_override = family;
     // The kernels compare row lengths against a 32-bit threshold; no row is
@@ -750,6 +820,17 @@ spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *
     return SPMM_OK;
 }
 
+spmm_status spmm_plan_prepare_blocks(spmm_plan_t plan, const int32_t *col, const float *val,
+                                     void *stream) {
+    if (!plan) return SPMM_ERR_INVALID_ARG;
+    Plan *p = reinterpret_cast<Plan *>(plan);
+    if (p->nnz > 0 && !col) return SPMM_ERR_INVALID_ARG;
+    if (p->row0 != 0) return SPMM_ERR_UNSUPPORTED;
+    if (col) col += p->col_base;
+    if (val) val += p->col_base;
+    return from_cuda(block_prepare(p, col, val, (cudaStream_t)stream));
+}
+
 spmm_status spmm_plan_sync(spmm_plan_t plan, void *stream) {
     if (!plan) return SPMM_ERR_INVALID_ARG;
     Plan *p = reinterpret_cast<Plan *>(plan);
@@ -816,6 +897,22 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
     a.act = (int32_t)act;
     a.rows_sorted = p->rows_sorted ? 1 : 0;
     a.row0 = p->row0;
+    a.seg_tiles = p->seg_tiles;
+    a.seg_n_tiles = p->seg_n_tiles;
+    if (r.family == SPMM_FAMILY_SEGMENT) {
+        spmm_status st = ensure_workspace(p, (size_t)r.workspace_bytes);
+        if (st != SPMM_OK) return st;
+        a.seg_warps = r.seg_warps;
+        char *wb = reinterpret_cast<char *>(p->work);
+        const size_t meta = ((size_t)r.seg_warps * sizeof(int4) + 255) / 256 * 256;
+        const size_t vals = (size_t)r.col_tiles * (size_t)r.seg_warps * 2 *
+                            (4 * (size_t)r.lanes * (size_t)r.seg_chunks) * 4;
+        a.seg_meta = reinterpret_cast<int4 *>(wb);
+        a.seg_cval = reinterpret_cast<float *>(wb + meta);
+        a.seg_carg = reduce == SPMM_MAX ? reinterpret_cast<int32_t *>(wb + meta + vals) : nullptr;
+        return from_cuda(launch_segment(a, r.lanes, r.seg_chunks, reduce, val != nullptr,
+                                        r.col_tiles, s));
+    }
     const bool split = p->n_heavy > 0 && r.family != SPMM_FAMILY_BLOCK;
     if (split) {
         spmm_status st = ensure_workspace(p, workspace_need(p, N, reduce));
@@ -829,6 +926,15 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
     const bool has_val = val != nullptr;
     cudaError_t e;
     if (r.family == SPMM_FAMILY_BLOCK) {
+        // A's diagonal blocks are prepared once per plan and flavour of A
+        if (p->bk_flavor != (has_val ? 1 : 0)) {
+            e = block_prepare(p, col, val, s);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+        a.bk_a = p->bk_tiles;
+        a.bk_off_rowptr = p->bk_off_rowptr;
+        a.bk_off_col = p->bk_off_col;
+        a.bk_off_val = p->bk_off_val;
         e = launch_block(a, reduce, has_val, s);
     } else if (r.family == SPMM_FAMILY_WINDOW) {
         WinShape w;

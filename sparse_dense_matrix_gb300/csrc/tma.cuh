@@ -103,6 +103,12 @@ __device__ __forceinline__ bool mbar_wait_poll(uint64_t *bar, uint32_t parity, i
     return false;
 }
 
+// Order this thread's earlier generic-proxy accesses of shared memory before its
+// later async-proxy ones (a bulk copy into a buffer that was just read).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Shared-memory loads by 32-bit shared-window address (volatile: they stay
 // after the mbarrier wait that publishes the data).
 __device__ __forceinline__ int lds_s32(uint32_t addr) {

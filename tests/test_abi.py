@@ -55,6 +55,7 @@ def test_host_argument_checks(sdm):
     assert lib.spmm_plan_reserve(None, 4, 0) == 1
     assert lib.spmm_plan_validate_cols(None, None, None) == 1
     assert lib.spmm_plan_sync(None, None) == 1
+    assert lib.spmm_plan_prepare_blocks(None, None, None, None) == 1
     info = sdm.PlanInfo()
     assert lib.spmm_plan_describe(None, 4, 0, ctypes.byref(info)) == 1
     assert lib.spmm_plan_set_family(None, 0, 0) == 1
@@ -90,7 +91,8 @@ def test_plan_create_without_a_gpu_reports_cuda_error(sdm):
 
 def _desc(M=1 << 20, nnz=10 << 20, cv=0.0, n_heavy=0, n_chunks=0, t_split=512):
     return dict(M=M, K=M, nnz=nnz, dbar=nnz / M, cv=cv, d_max=10, n_empty=0,
-                t_split=t_split, chunk=t_split // 2, n_heavy=n_heavy, n_chunks=n_chunks)
+                t_split=t_split, chunk=t_split // 2, n_heavy=n_heavy, n_chunks=n_chunks,
+                seg_tiles=(M + nnz + 543) // 544)
 
 
 def test_router_rules(sdm):
@@ -120,6 +122,30 @@ def test_router_rules(sdm):
     assert (r["vec"], r["lanes"], r["rows_per_warp"]) == (1, 2, 16)
     r = sdm.spmm_route(_desc(cv=0.0), 16, 0, family=sdm.FAMILY["warprow"])
     assert r["family_name"] == "warprow"
+
+
+def test_router_segment_rule(sdm):
+    """Skewed degrees at N <= 16 with 128-bit vectors and aligned col/val go to
+    the merge-path SEGMENT family: two launches, no split-row launches, a
+    workspace of two partial rows per warp (+ a 16-byte record per warp)."""
+    d = _desc(M=1 << 22, nnz=104_839_949, cv=20.6, n_heavy=9000, n_chunks=90000)
+    for N in (4, 8, 16):
+        r = sdm.spmm_route(d, N, 0, aligned=3)
+        assert r["family_name"] == "segment", N
+        assert r["launches"] == 2 and r["seg_warps"] == 152 * 16 and r["col_tiles"] == 1
+    r = sdm.spmm_route(d, 16, 0, aligned=3)
+    assert r["workspace_bytes"] == 152 * 16 * 16 + 152 * 16 * 2 * 16 * 4
+    r = sdm.spmm_route(d, 16, 2, aligned=3)                    # + argmax partials
+    assert r["workspace_bytes"] == 152 * 16 * 16 + 2 * 152 * 16 * 2 * 16 * 4
+    assert sdm.spmm_route(d, 16, 0, aligned=1)["family_name"] == "warprow"   # col/val unaligned
+    assert sdm.spmm_route(d, 64, 0, aligned=3)["family_name"] == "warprow"   # wider N
+    assert sdm.spmm_route(d, 18, 0, aligned=3)["family_name"] == "warprow"   # no 128-bit vectors
+    assert sdm.spmm_route(_desc(cv=0.5), 16, 0, aligned=3)["family_name"] == "rowgroup"
+    pin = sdm.FAMILY["segment"]
+    r = sdm.spmm_route(d, 1000, 0, aligned=3, family=pin)      # two chunks per lane, 4 tiles
+    assert (r["family_name"], r["lanes"], r["seg_chunks"], r["col_tiles"]) == ("segment", 32, 2, 4)
+    assert r["seg_warps"] == 152 // 4 * 16
+    assert sdm.spmm_route(d, 6, 0, aligned=3, family=pin)["family_name"] == "warprow"
 
 
 def test_router_split_launches_and_workspace(sdm):
