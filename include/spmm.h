@@ -212,9 +212,11 @@ spmm_status spmm_partition_rows(const int32_t *rowptr, int64_t M, int32_t parts,
  *   argmax : device, int32 [M, N] (SPMM_MAX only; may be NULL to skip it).
  * 128-bit loads are used when N % 4 == 0 and B and C are 16-byte aligned;
  * otherwise the scalar path runs (same results). Grows the plan's workspace
- * with cudaMalloc when the heavy-row split needs more than it holds (use
- * spmm_plan_reserve beforehand to keep allocation out of timed or captured
- * regions).
+ * with cudaMalloc when the heavy-row split or the SEGMENT family's open rows
+ * need more than it holds (use spmm_plan_reserve beforehand to keep
+ * allocation out of timed or captured regions), and the first BLOCK product
+ * prepares the plan's diagonal blocks (spmm_plan_prepare_blocks beforehand
+ * does the same).
  * (ParamSpMM section 2, Algorithm 1; graph-spmm model card, "Method".)
  */
 spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, const float *B,

@@ -423,7 +423,9 @@ spmm_status plan_ensure_workspace(Plan *p, size_t need) { return ensure_workspac
 //       lane group preferred, else one), a 2W halo at most twice a CTA's
 //       row range, and (row-range plans) a first row on a multiple of the
 //       tile's R rows                                          -> WINDOW;
-//   R1a BLOCK (tensor cores) only when pinned;
+//   R1a block-diagonal graphs (>= 85% of the entries in their row's
+//       256-column diagonal block, blocks >= 5% dense), sum or mean,
+//       N % 16 == 0, aligned B/C, a whole-matrix plan     -> BLOCK (tensor cores);
 //   R2  wide N (more than 32 column vectors per row)        -> WARPROW with column
 //       tiles (COLTILE, the staged variant, measured 1.1-1.7x slower: pin only);
 //   R3  skewed degrees (CV_d > 1), N <= 16 in 128-bit vectors, col/val
@@ -455,14 +457,18 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     const bool window_ok = (family_override == SPMM_FAMILY_AUTO || forced) &&
                            d->band_w > 0 && (aligned & 3) == 3 && N > 0 && N % 4 == 0 &&
                            (forced || (d->dbar >= 2.0 && d->band_cover >= 0.97)) && d->M > 0;
-    // R1a: BLOCK (tensor cores) only when pinned. It is correct on any graph,
-    // but on the 64k-row community graph (51 of 56 entries per row inside the
-    // 256-column diagonal blocks, block density 0.2) it measured 145 us at
-    // N=128 against 94 us for WARPROW: the per-chunk staging of the operands,
-    // not the tensor cores, bounds it. The router keeps it out until it wins.
-    // Its diagonal blocks are those of a plan that starts at row 0.
-    if (family_override == SPMM_FAMILY_BLOCK && d->M > 0 && N > 0 && N % 16 == 0 &&
-        (aligned & 1) && reduce != SPMM_MAX && d->row0 == 0)
+    // R1a: BLOCK (tensor cores) when pinned, or when at least 85% of the
+    // entries lie in their row's 256-column diagonal block and those blocks
+    // are at least 5% dense (known after the column check). On the 64k-row
+    // community graph (91% of the entries in blocks of density 0.2) it
+    // measured 81.9 us at N=128 and 271 us at N=512, against 96.5 and 338 us
+    // for WARPROW. Its diagonal blocks are those of a plan that starts at row 0.
+    const bool block_shape = d->M > 0 && N > 0 && N % 16 == 0 && (aligned & 1) &&
+                             reduce != SPMM_MAX && d->row0 == 0;
+    const bool block_dense = d->nnz > 0 && (double)d->blk_intra >= 0.85 * (double)d->nnz &&
+                             (double)d->blk_intra >= 0.05 * (double)d->M * kBlockRows;
+    if (block_shape && (family_override == SPMM_FAMILY_BLOCK ||
+                        (family_override == SPMM_FAMILY_AUTO && block_dense)))
         fam = SPMM_FAMILY_BLOCK;
     int64_t win_tiles = 0;
     if (window_ok && fam == -2) {
@@ -766,7 +772,12 @@ spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split) 
 spmm_status spmm_plan_reserve(spmm_plan_t plan, int64_t N, spmm_reduce reduce) {
     if (!plan || N < 0 || reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
     Plan *p = reinterpret_cast<Plan *>(plan);
-    return ensure_workspace(p, workspace_need(p, N, reduce));
+    // the larger of the split-row partials and the SEGMENT family's open rows
+    spmm_plan_info r;
+    fill_desc(p, &r);
+    route_fill(&r, N, reduce, 7, p->num_sms, SPMM_FAMILY_SEGMENT, &r);
+    const size_t seg = r.family == SPMM_FAMILY_SEGMENT ? (size_t)r.workspace_bytes : 0;
+    return ensure_workspace(p, std::max(workspace_need(p, N, reduce), seg));
 }
 
 spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *stream) {

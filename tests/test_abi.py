@@ -208,11 +208,18 @@ def test_router_window_rule(sdm):
 
 
 def test_router_block_rule(sdm):
-    # community 64k: 256 blocks of 256 rows, 51 of 56 entries per row inside the block;
-    # BLOCK is used only when pinned (it measured slower than WARPROW there)
+    # community 64k: 256 blocks of 256 rows, 51 of 56 entries per row inside the
+    # block (91%, block density 0.2): routed to BLOCK for sum and mean
     com = dict(_desc(M=65536, nnz=3668321, cv=0.1), band_w=256, band_cover=0.91,
                rows_sorted=1, blk_intra=3342000)
-    assert sdm.spmm_route(com, 128, 0)["family_name"] != "block"
+    assert sdm.spmm_route(com, 128, 0)["family_name"] == "block"
+    assert sdm.spmm_route(com, 512, 1)["family_name"] == "block"
+    assert sdm.spmm_route(com, 128, 2)["family_name"] != "block"                # max
+    assert sdm.spmm_route(dict(com, blk_intra=0), 128, 0)["family_name"] != "block"  # unknown
+    assert sdm.spmm_route(dict(com, blk_intra=3000000), 128, 0)["family_name"] != "block"  # 82%
+    sparse_blocks = dict(_desc(M=65536, nnz=500000, cv=0.1), blk_intra=480000)   # 2.9% dense
+    assert sdm.spmm_route(sparse_blocks, 128, 0)["family_name"] != "block"
+    assert sdm.spmm_route(com, 128, 0, family=sdm.FAMILY["warprow"])["family_name"] == "warprow"
     pin = sdm.FAMILY["block"]
     r = sdm.spmm_route(com, 128, 0, family=pin)
     assert (r["family_name"], r["col_tiles"], r["launches"]) == ("block", 1, 1)

@@ -82,7 +82,10 @@ def test_block_descriptors_and_pinning(sdm, cuda_device):
     adj = make_adj(sdm, g, cuda_device)
     info = adj.describe(128, "sum")
     assert info["rows_sorted"] == 1 and info["blk_intra"] > 0.85 * g.nnz
-    assert info["family_name"] != "block"                          # pinned only
+    assert info["family_name"] == "block"                          # routed
+    assert info["block_bytes"] == 0                                 # prepared on first use
+    adj.set_family("warprow")
+    assert adj.describe(128, "sum")["family_name"] == "warprow"
     adj.set_family("block")
     info = adj.describe(128, "sum")
     assert info["family_name"] == "block" and info["launches"] == 1
@@ -91,6 +94,35 @@ def test_block_descriptors_and_pinning(sdm, cuda_device):
     B = gen.features(g.K, 128, seed=5)
     C, A = gpu_reduce(adj, to_dev(B, cuda_device), "max")
     compare(g, B, "max", C, A, label="community max (SIMT)")
+    # preparation: explicit, then reported; 256 KB per 128-row tile + the
+    # compact CSR of the entries outside the diagonal blocks
+    sdm.spmm_plan_prepare_blocks(adj.plan, adj.col.data_ptr(), adj.val.data_ptr())
+    n_off = g.nnz - info["blk_intra"]
+    want = (g.M + 127) // 128 * 256 * 1024 + 4 * (g.M + 1) + 8 * n_off
+    assert adj.describe(128, "sum")["block_bytes"] == want
+    C, A = gpu_reduce(adj, to_dev(B, cuda_device), "sum")
+    compare(g, B, "sum", C, A, label="community sum after explicit preparation")
+    adj.close()
+
+
+def test_block_reprepares_for_the_other_flavour(sdm, cuda_device):
+    """The prepared pieces belong to one flavour of A (weighted or not): a run
+    with the other flavour prepares again, and every run stays correct."""
+    import torch
+    g = graph("community")
+    adj = make_adj(sdm, g, cuda_device)
+    adj.set_family("block")
+    N = 64
+    B = gen.features(g.K, N, seed=6)
+    Bd = to_dev(B, cuda_device)
+    Cd = torch.empty((g.M, N), dtype=torch.float32, device=cuda_device)
+    for weighted in (True, False, True):
+        gg = g if weighted else unweighted(g)
+        sdm.spmm_run(adj.plan, adj.col.data_ptr(), adj.val.data_ptr() if weighted else None,
+                     Bd.data_ptr(), N, sdm.REDUCE["sum"], Cd.data_ptr())
+        torch.cuda.synchronize()
+        compare(gg, B, "sum", Cd.cpu().numpy(), None,
+                label=f"block {'weighted' if weighted else 'unweighted'}")
     adj.close()
 
 

@@ -1,8 +1,9 @@
 """spmm_run inside a CUDA graph: capture, replay, same bits as the eager call.
 
 Every family's launch is a plain kernel launch on the caller's stream (the
-tensor maps are encoded on the host and passed by value, the split-row
-workspace is reserved beforehand), so a product can be captured once and
+tensor maps are encoded on the host and passed by value, the split-row and
+open-row workspace is reserved beforehand, BLOCK's diagonal blocks are
+prepared by the eager call), so a product can be captured once and
 replayed. The replayed results must equal the eager ones bit for bit, and the
 eager ones are held to the oracle as in the other parity tests.
 """
@@ -28,6 +29,8 @@ CASES = [
     ("rmat", 128, "max", None),
     ("er", 32, "max", None),            # ROWGROUP
     ("community", 128, "sum", "block"),
+    ("rmat", 16, "sum", "segment"),     # merge-path tiles + the open-row launch
+    ("rmat", 16, "max", "segment"),
 ]
 GRAPHS = {
     "knn": lambda: gen.knn_local(20000, 10, 64, seed=31),
