@@ -147,6 +147,7 @@ struct RunArgs {
     const int32_t *__restrict__ bk_off_rowptr;
     const int32_t *__restrict__ bk_off_col;
     const float *__restrict__ bk_off_val;
+    float *bk_p;                              // [M][N] off-block partial rows (workspace)
 };
 
 // Fused epilogue on V consecutive outputs starting at column c: C = act(C + bias).

@@ -20,11 +20,13 @@
 //     accumulator in tensor memory: a_hi b_hi + a_hi b_lo + a_lo b_hi (about
 //     2^-21 relative per term; two passes for an unweighted A, whose lo is 0)
 //     and commits each chunk to the stage's "free" barrier.
-// The three roles overlap across the two stages. The epilogue reads the
-// accumulator back through shared memory and finishes the rows
-// warp-cooperatively: the row's entries outside the block in CSR order (fp32
-// FMA), the mean's 1/d, the fused bias/ReLU, one store of C. Sum and mean only
-// (max needs comparisons, not products). Operand tiles are K-major without
+// The three roles overlap across the two stages. Meanwhile warps 8-15 take
+// the rows' entries outside the diagonal block (lanes across the tile's
+// columns, fp32 FMA in CSR order from zero) and write each row's partial to
+// the workspace P. The epilogue reads the accumulator back through shared
+// memory and finishes the rows warp-cooperatively: block sum + P, the mean's
+// 1/d, the fused bias/ReLU, one store of C. Sum and mean only (max needs
+// comparisons, not products). Operand tiles are K-major without
 // swizzle: 8-row x 16-byte core matrices, 128 bytes apart along K and
 // (KC / 4) * 128 bytes apart along rows.
 #include <cstring>
@@ -39,7 +41,8 @@ namespace spmm {
 
 namespace {
 
-constexpr int kBkThreads = 256;
+constexpr int kBkThreads = 512;              // warps 0-7: the product; 8-15: off-block rows
+constexpr int kBkMainWarps = 8;
 constexpr int kBkM = 128;                    // rows per CTA (MMA M)
 constexpr int kBkN = 128;                    // output columns per CTA (MMA N, TMEM columns)
 constexpr int kBkKC = 16;                    // block columns per chunk
@@ -52,12 +55,7 @@ constexpr int kBkStages = 2;
 // per stage: A hi, A lo, B as loaded, B hi, B lo
 constexpr uint32_t kStageBytes = 2 * kPiece + 3 * kBTile;
 constexpr uint32_t kOffBars = kBkStages * kStageBytes;
-// the CTA's entries outside the diagonal block, staged during the main loop
-constexpr int kOffCap = 1536;
-constexpr uint32_t kOffORp = kOffBars + 128;                 // int [kBkM + 1]
-constexpr uint32_t kOffOCol = kOffORp + (kBkM + 1 + 3) / 4 * 16;
-constexpr uint32_t kOffOVal = kOffOCol + kOffCap * 4;
-constexpr int kBkSmem = (int)(kOffOVal + kOffCap * 4) + 1024;
+constexpr int kBkSmem = (int)kOffBars + 128 + 1024;
 constexpr int kTilePitch = kBkN + 4;         // accumulator rows in shared memory (floats)
 constexpr int kConvThreads = 4 * kWarp;      // warps 4-7
 static_assert(kBkM * kTilePitch * 4 <= (int)kOffBars, "the accumulator tile reuses the stages");
@@ -195,19 +193,70 @@ __global__ void __launch_bounds__(kBkThreads, 2) k_block(const RunArgs a,
                     smem_addr(&done[s]))
                 : "memory");
         }
-    } else if (warp == 2 || warp == 3) {
-        // ------------------------------------- off-block entries to shared memory
-        int *orp = reinterpret_cast<int *>(sm + kOffORp);
-        int *ocol = reinterpret_cast<int *>(sm + kOffOCol);
-        float *oval = reinterpret_cast<float *>(sm + kOffOVal);
-        const int i = t - 2 * kWarp;                      // 0..63
+    } else if (warp >= kBkMainWarps) {
+        // ------------------------------------------- rows' off-block entries
+        // Meanwhile the other eight warps take the rows' entries outside the
+        // diagonal block (lanes across the tile's columns, two rows at a time,
+        // up to three entries of each per step: six gathers in flight per
+        // lane), sum them in CSR order from zero and write the partial row to
+        // the workspace P, which the epilogue adds to the block's sum.
+        const int cl = 4 * lane;
+        const bool col_ok = cl < n_eff;
+        const float *Bc = a.B + n0 + (col_ok ? cl : 0);
         const int nrows = (int)(a.M - r0 < kBkM ? a.M - r0 : kBkM);
-        const int q0 = a.bk_off_rowptr[r0];
-        for (int k = i; k <= nrows; k += 2 * kWarp) orp[k] = a.bk_off_rowptr[r0 + k] - q0;
-        const int n_off = min(a.bk_off_rowptr[r0 + nrows] - q0, kOffCap);
-        for (int k = i; k < n_off; k += 2 * kWarp) {
-            ocol[k] = __ldg(a.bk_off_col + q0 + k);
-            if (HAS_VAL) oval[k] = __ldg(a.bk_off_val + q0 + k);
+        constexpr int kWW = kBkThreads / kWarp - kBkMainWarps;   // worker warps
+        constexpr int kRB = 2, kEB = 3;
+        for (int rr0 = warp - kBkMainWarps; rr0 < nrows; rr0 += kRB * kWW) {
+            int qa[kRB], qb[kRB];
+            float4 acc[kRB];
+#pragma unroll
+            for (int k = 0; k < kRB; ++k) {
+                const int rr = rr0 + k * kWW;
+                const bool live = rr < nrows;
+                qa[k] = live ? a.bk_off_rowptr[r0 + rr] : 0;
+                qb[k] = live ? a.bk_off_rowptr[r0 + rr + 1] : 0;
+                acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            bool more = qa[0] < qb[0] || qa[1] < qb[1];
+            while (more) {                                  // uniform across the warp
+                int j[kRB][kEB];
+                float w[kRB][kEB];
+                float4 x[kRB][kEB];
+#pragma unroll
+                for (int k = 0; k < kRB; ++k)
+#pragma unroll
+                    for (int u = 0; u < kEB; ++u) {
+                        const bool in = qa[k] + u < qb[k];
+                        j[k][u] = in ? __ldg(a.bk_off_col + qa[k] + u) : 0;
+                        w[k][u] = (HAS_VAL && in) ? __ldg(a.bk_off_val + qa[k] + u) : 1.0f;
+                    }
+#pragma unroll
+                for (int k = 0; k < kRB; ++k)
+#pragma unroll
+                    for (int u = 0; u < kEB; ++u)
+                        if (qa[k] + u < qb[k])
+                            x[k][u] = __ldg(reinterpret_cast<const float4 *>(Bc + (int64_t)j[k][u] * N));
+                more = false;
+#pragma unroll
+                for (int k = 0; k < kRB; ++k) {
+#pragma unroll
+                    for (int u = 0; u < kEB; ++u)
+                        if (qa[k] + u < qb[k]) {
+                            acc[k].x = __fmaf_rn(w[k][u], x[k][u].x, acc[k].x);
+                            acc[k].y = __fmaf_rn(w[k][u], x[k][u].y, acc[k].y);
+                            acc[k].z = __fmaf_rn(w[k][u], x[k][u].z, acc[k].z);
+                            acc[k].w = __fmaf_rn(w[k][u], x[k][u].w, acc[k].w);
+                        }
+                    qa[k] += kEB;
+                    more |= qa[k] < qb[k];
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kRB; ++k) {
+                const int rr = rr0 + k * kWW;
+                if (rr < nrows && col_ok)
+                    *reinterpret_cast<float4 *>(a.bk_p + (r0 + rr) * N + n0 + cl) = acc[k];
+            }
         }
     } else if (warp >= 4) {
         // ---------------------------------------------------------- B split
@@ -262,7 +311,7 @@ __global__ void __launch_bounds__(kBkThreads, 2) k_block(const RunArgs a,
         float *tile_s = reinterpret_cast<float *>(sm);      // [kBkM][kTilePitch]
         const int rl = (warp & 3) * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        for (int c = (warp >> 2) * 16; c < n_eff; c += 32) {
+        for (int c = (warp >> 2) * 16; c < n_eff; c += 16 * (kBkThreads / kWarp / 4)) {
             float v[16];
             tmem_ld16(trow + (uint32_t)c, v);
             float4 *dst = reinterpret_cast<float4 *>(tile_s + rl * kTilePitch + c);
@@ -271,86 +320,29 @@ __global__ void __launch_bounds__(kBkThreads, 2) k_block(const RunArgs a,
                 dst[e4] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
         }
         __syncthreads();
-        // Rows are finished four at a time per warp (rows rr0 + 8 k), up to
-        // kEB entries of each in one step: twelve gathers in flight per lane
-        // (the register budget of two CTAs per SM).
-        // The entries come from the staged copy (the first kOffCap of the
-        // CTA), else from global memory.
-        const int *orp = reinterpret_cast<const int *>(sm + kOffORp);
-        const int *ocol = reinterpret_cast<const int *>(sm + kOffOCol);
-        const float *oval = reinterpret_cast<const float *>(sm + kOffOVal);
-        const int q0g = a.bk_off_rowptr[r0];
-        const int cl = 4 * lane;                            // this lane's 4 columns
+        // each warp finishes rows warp, warp + 16, ...: the block's sum plus
+        // the off-block partial P (written by this CTA's worker warps; plain
+        // coherent loads, ordered by the barrier above), mean, bias/ReLU
+        const int cl = 4 * lane;
         const bool col_ok = cl < n_eff;
         const int cc = col_ok ? cl : 0;
-        const float *Bc = a.B + n0 + cc;
         const int nrows = (int)(a.M - r0 < kBkM ? a.M - r0 : kBkM);
-        constexpr int kRB = 4;                              // rows per batch
-        constexpr int kEB = 3;                              // entries per row per step
-        for (int rr0 = warp; rr0 < nrows; rr0 += kRB * (kBkThreads / kWarp)) {
-            int qa[kRB], qb[kRB];
-            float4 acc[kRB];
+        for (int rr = warp; rr < nrows; rr += kBkThreads / kWarp) {
+            const int64_t i = r0 + rr;
+            const float4 bsum = *reinterpret_cast<const float4 *>(tile_s + rr * kTilePitch + cc);
+            float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (col_ok) pv = *reinterpret_cast<const float4 *>(a.bk_p + i * N + n0 + cl);
+            float out[4] = {__fadd_rn(bsum.x, pv.x), __fadd_rn(bsum.y, pv.y),
+                            __fadd_rn(bsum.z, pv.z), __fadd_rn(bsum.w, pv.w)};
+            if (RED == SPMM_MEAN) {
+                const int d = a.rowptr[i + 1] - a.rowptr[i];
+                const float inv_d = d > 0 ? rcp_approx((float)d) : 0.0f;
 #pragma unroll
-            for (int k = 0; k < kRB; ++k) {
-                const int rr = rr0 + k * (kBkThreads / kWarp);
-                const bool live = rr < nrows;
-                qa[k] = live ? orp[rr] : 0;
-                qb[k] = live ? orp[rr + 1] : 0;
-                acc[k] = live ? *reinterpret_cast<const float4 *>(tile_s + rr * kTilePitch + cc)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int e = 0; e < 4; ++e) out[e] = __fmul_rn(out[e], inv_d);
             }
-            bool more = true;
-            while (more) {                                  // uniform across the warp
-                int j[kRB][kEB];
-                float w[kRB][kEB];
-                float4 x[kRB][kEB];
-#pragma unroll
-                for (int k = 0; k < kRB; ++k)
-#pragma unroll
-                    for (int u = 0; u < kEB; ++u) {
-                        const int q = qa[k] + u;
-                        const bool in = q < qb[k];
-                        j[k][u] = !in ? 0 : q < kOffCap ? ocol[q] : __ldg(a.bk_off_col + q0g + q);
-                        w[k][u] = (!HAS_VAL || !in) ? 1.0f
-                                  : q < kOffCap ? oval[q] : __ldg(a.bk_off_val + q0g + q);
-                    }
-#pragma unroll
-                for (int k = 0; k < kRB; ++k)
-#pragma unroll
-                    for (int u = 0; u < kEB; ++u)
-                        if (qa[k] + u < qb[k])
-                            x[k][u] = __ldg(reinterpret_cast<const float4 *>(Bc + (int64_t)j[k][u] * N));
-                more = false;
-#pragma unroll
-                for (int k = 0; k < kRB; ++k) {
-#pragma unroll
-                    for (int u = 0; u < kEB; ++u)
-                        if (qa[k] + u < qb[k]) {
-                            acc[k].x = __fmaf_rn(w[k][u], x[k][u].x, acc[k].x);
-                            acc[k].y = __fmaf_rn(w[k][u], x[k][u].y, acc[k].y);
-                            acc[k].z = __fmaf_rn(w[k][u], x[k][u].z, acc[k].z);
-                            acc[k].w = __fmaf_rn(w[k][u], x[k][u].w, acc[k].w);
-                        }
-                    qa[k] += kEB;
-                    more |= qa[k] < qb[k];
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < kRB; ++k) {
-                const int rr = rr0 + k * (kBkThreads / kWarp);
-                if (rr >= nrows) break;
-                const int64_t i = r0 + rr;
-                float out[4] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w};
-                if (RED == SPMM_MEAN) {
-                    const int d = a.rowptr[i + 1] - a.rowptr[i];
-                    const float inv_d = d > 0 ? rcp_approx((float)d) : 0.0f;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) out[e] = __fmul_rn(out[e], inv_d);
-                }
-                if (col_ok) {
-                    epilogue<4>(a, (int64_t)n0 + cl, out);
-                    st_vec<4>(a.C + i * N + n0 + cl, out);
-                }
+            if (col_ok) {
+                epilogue<4>(a, (int64_t)n0 + cl, out);
+                st_vec<4>(a.C + i * N + n0 + cl, out);
             }
         }
     } else if (t == 0) {

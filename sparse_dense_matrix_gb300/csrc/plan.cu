@@ -551,6 +551,12 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     o->rows_per_warp = fam == SPMM_FAMILY_ROWGROUP ? (int32_t)(32 / lanes) : 1;
     o->seg_warps = 0;
     o->seg_chunks = 0;
+    if (fam == SPMM_FAMILY_BLOCK) {
+        // the off-block partial rows, [M][N] fp32
+        o->launches = (d->M > 0 && N > 0) ? 1 : 0;
+        o->workspace_bytes = d->M * N * 4;
+        return;
+    }
     if (fam == SPMM_FAMILY_SEGMENT) {
         // every row, however long, goes through the merge-path tiles: no split
         o->seg_chunks = (int32_t)seg_q;
@@ -777,7 +783,11 @@ spmm_status spmm_plan_reserve(spmm_plan_t plan, int64_t N, spmm_reduce reduce) {
     fill_desc(p, &r);
     route_fill(&r, N, reduce, 7, p->num_sms, SPMM_FAMILY_SEGMENT, &r);
     const size_t seg = r.family == SPMM_FAMILY_SEGMENT ? (size_t)r.workspace_bytes : 0;
-    return ensure_workspace(p, std::max(workspace_need(p, N, reduce), seg));
+    // and the BLOCK family's off-block partial rows when it is the routed family
+    fill_desc(p, &r);
+    route_fill(&r, N, reduce, 7, p->num_sms, p->family_override, &r);
+    const size_t blk = r.family == SPMM_FAMILY_BLOCK ? (size_t)r.workspace_bytes : 0;
+    return ensure_workspace(p, std::max(std::max(workspace_need(p, N, reduce), seg), blk));
 }
 
 spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *stream) {
@@ -942,6 +952,9 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
             e = block_prepare(p, col, val, s);
             if (e != cudaSuccess) return from_cuda(e);
         }
+        spmm_status st = ensure_workspace(p, (size_t)r.workspace_bytes);
+        if (st != SPMM_OK) return st;
+        a.bk_p = reinterpret_cast<float *>(p->work);
         a.bk_a = p->bk_tiles;
         a.bk_off_rowptr = p->bk_off_rowptr;
         a.bk_off_col = p->bk_off_col;
