@@ -45,6 +45,10 @@ METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
 # family's sources then (family_sources_sha256()), and the bench reports the
 # traffic as null once they differ.
 NCU_TRAFFIC = {
+    # the light-row launch k_warprow<4,32,MAX,weighted> (rows of at most 512
+    # entries) at full size; the split rows' two launches are not included
+    "warprow/chung_lu_4M/N256/max": {"bytes": 34785350912 + 9294084608, "sources_sha256":
+                                     "1e9d81c29cfbc6e05de6e58ce6a113560561c89ea5d4f55061f5b099c767d3be"},
     "window/knn_1M/N16/sum": {"bytes": 149.09e6, "sources_sha256":
                               "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af"},
     "window/knn_1M/N16/mean": {"bytes": 148.67e6, "sources_sha256":
@@ -61,8 +65,11 @@ FAMILY_SOURCES = {
     "window": (_CSRC + "common.cuh", _CSRC + "tma.cuh", _CSRC + "window.cuh",
                _CSRC + "f_window.cu", _CSRC + "f_window_sum.cu", _CSRC + "f_window_mean.cu",
                _CSRC + "f_window_max.cu", "include/spmm.h"),
-    "warprow": (_CSRC + "common.cuh", _CSRC + "f_warprow.cu", _CSRC + "plan.cu",
+    "warprow": (_CSRC + "common.cuh", _CSRC + "f_warprow.cu", "include/spmm.h"),
+    "segment": (_CSRC + "common.cuh", _CSRC + "tma.cuh", _CSRC + "segment.cuh",
+                _CSRC + "f_segment.cu", _CSRC + "f_segment_sum.cu", _CSRC + "f_segment_max.cu",
                 "include/spmm.h"),
+    "block": (_CSRC + "common.cuh", _CSRC + "tma.cuh", _CSRC + "f_block.cu", "include/spmm.h"),
 }
 
 
@@ -540,6 +547,9 @@ def run_ours(args):
                 "frac": achieved / hbm_peak, "frac_nominal": achieved / NOMINAL_HBM_GBS,
                 "nominal_peak": NOMINAL_HBM_GBS, "duration": "median of the run's steps",
                 "traffic": ncu_traffic(key, info["family_name"]),
+                "traffic_scope": "dram__bytes_read.sum + dram__bytes_write.sum of the run's "
+                                 "main launch (for WARPROW the light rows; its split-row "
+                                 "launches are not included), one ncu capture",
                 "kernel": key, "peak_source": peak_kind,
                 "algorithmic_bytes_per_launch": bytes_dom,
                 "launches_per_run": info["launches"]}
