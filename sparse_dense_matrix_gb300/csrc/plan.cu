@@ -428,7 +428,7 @@ spmm_status plan_ensure_workspace(Plan *p, size_t need) { return ensure_workspac
 //       N % 16 == 0, aligned B/C, a whole-matrix plan     -> BLOCK (tensor cores);
 //   R2  wide N (more than 32 column vectors per row)        -> WARPROW with column
 //       tiles (COLTILE, the staged variant, measured 1.1-1.7x slower: pin only);
-//   R3  skewed degrees (CV_d > 1), N <= 16 in 128-bit vectors, col/val
+//   R3  skewed degrees (CV_d > 1), N <= 32 in 128-bit vectors, col/val
 //       16-byte aligned                                       -> SEGMENT (merge-path tiles);
 //   R4  near-uniform degrees (CV_d <= 1) and narrow N (L < 32 lanes, so
 //       several rows share a warp)                            -> ROWGROUP, 32/L rows per warp;
@@ -523,12 +523,13 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
             fam = family_override;
         else if (n_vec > 32)
             fam = SPMM_FAMILY_WARPROW;   // measured faster than COLTILE on the wide workloads
-        else if (segment_ok && d->cv > 1.0 && n_vec <= 4)
-            // skewed degrees at narrow N (four lanes or fewer per entry): the
+        else if (segment_ok && d->cv > 1.0 && n_vec <= 8)
+            // skewed degrees at narrow N (eight lanes or fewer per entry): the
             // merge-path tiles keep every lane's gathers in flight where a warp
             // per row waits on short rows (Chung-Lu 4M, N=16: 1.37 against
-            // 1.71 ms for the sum, 1.81 against 2.24 ms for max); at N=64 and
-            // wider WARPROW measured 8-40% faster
+            // 1.71 ms for the sum, 1.81 against 2.24 ms for max; N=32: 2.08
+            // against 2.17 ms, 2.70 against 2.99 ms); at N=64 and wider
+            // WARPROW measured 8-40% faster
             fam = SPMM_FAMILY_SEGMENT;
         else if (d->cv <= 1.0 && lanes < 32)
             // a 32-lane ROWGROUP holds one row per warp like WARPROW, without

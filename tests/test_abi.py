@@ -125,11 +125,11 @@ def test_router_rules(sdm):
 
 
 def test_router_segment_rule(sdm):
-    """Skewed degrees at N <= 16 with 128-bit vectors and aligned col/val go to
+    """Skewed degrees at N <= 32 with 128-bit vectors and aligned col/val go to
     the merge-path SEGMENT family: two launches, no split-row launches, a
     workspace of two partial rows per warp (+ a 16-byte record per warp)."""
     d = _desc(M=1 << 22, nnz=104_839_949, cv=20.6, n_heavy=9000, n_chunks=90000)
-    for N in (4, 8, 16):
+    for N in (4, 8, 16, 32):
         r = sdm.spmm_route(d, N, 0, aligned=3)
         assert r["family_name"] == "segment", N
         assert r["launches"] == 2 and r["seg_warps"] == 152 * 16 and r["col_tiles"] == 1
