@@ -141,7 +141,9 @@ typedef struct {
  *   out    : receives the plan (left NULL on error).
  * Computes, in one pass over rowptr, the degree descriptors (M, nnz, mean
  * degree, degree CV, max degree, empty rows) and the list of heavy rows that
- * spmm_run splits across CTAs. Returns SPMM_ERR_INVALID_INPUT when rowptr[0]
+ * spmm_run splits across CTAs, and, by a binary search per tile, the SEGMENT
+ * family's merge-path tile table (the rows ended and entries consumed at every
+ * 544th item of entries plus row ends; 8 bytes per tile). Returns SPMM_ERR_INVALID_INPUT when rowptr[0]
  * != 0 or rowptr decreases anywhere (checked on the device; no trap).
  * (RA-SpMM abstract: descriptors in O(M); graph-spmm model card, "API":
  * SparseAdj is held once and applied many times.)
