@@ -42,21 +42,22 @@ METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # family's kernels on a workload run, from one ncu capture. The counters belong
 # to the kernel build they were taken on: "sources_sha256" is the sha256 of the
-# family's sources then (family_sources_sha256()), and the bench reports the
-# traffic as null once they differ.
+# family's sources then, comments and white space left out
+# (family_sources_sha256()), and the bench reports the traffic as null once
+# they differ.
 NCU_TRAFFIC = {
     # the light-row launch k_warprow<4,32,MAX,weighted> (rows of at most 512
     # entries) at full size; the split rows' two launches are not included
     "warprow/chung_lu_4M/N256/max": {"bytes": 34785350912 + 9294084608, "sources_sha256":
-                                     "1e9d81c29cfbc6e05de6e58ce6a113560561c89ea5d4f55061f5b099c767d3be"},
+                                     "8200afc07d8b52fe1ffdc18676eec73996e7697cf568587645670b9c2c5ab84d"},
     "window/knn_1M/N16/sum": {"bytes": 149.09e6, "sources_sha256":
-                              "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af"},
+                              "1fe0fed1f8a2523e915205ee6a9478189195e9348ad39b178ca0ae705ed85a50"},
     "window/knn_1M/N16/mean": {"bytes": 148.67e6, "sources_sha256":
-                               "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af"},
+                               "1fe0fed1f8a2523e915205ee6a9478189195e9348ad39b178ca0ae705ed85a50"},
     "window/knn_1M/N64/sum": {"bytes": 557.30e6, "sources_sha256":
-                              "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af"},
+                              "1fe0fed1f8a2523e915205ee6a9478189195e9348ad39b178ca0ae705ed85a50"},
     "window/knn_1M/N64/mean": {"bytes": 559.95e6, "sources_sha256":
-                               "d1d27f0b5f9d37b62bf1f9ab0f188597bfa7a1d1fb4ce5bbe2550aa764b231af"},
+                               "1fe0fed1f8a2523e915205ee6a9478189195e9348ad39b178ca0ae705ed85a50"},
 }
 
 _CSRC = "sparse_dense_matrix_gb300/csrc/"
@@ -73,12 +74,37 @@ FAMILY_SOURCES = {
 }
 
 
+def _code_only(text):
+    """C/C++/CUDA source without its comments, white space runs collapsed."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":                       # string or character literal, kept
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def family_sources_sha256(family):
     h = hashlib.sha256()
     for rel in FAMILY_SOURCES.get(family, ()):
         h.update(rel.encode())
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

@@ -41,3 +41,15 @@ def test_default_workload_is_the_largest(monkeypatch):
     assert gen.CONFIGS[5]["name"] == "chung_lu_4M"
     assert bench.DEFAULT_N[5] == (16, 64, 256)
     assert set(gen.CONFIGS[5]["reduce"]) == {"sum", "mean", "max"}
+
+
+def test_traffic_key_ignores_comments_only():
+    """The DRAM traffic recorded for a kernel build stays valid across comment
+    and layout edits, and no longer applies once the code changes."""
+    import bench
+    a = 'int a; // one\n/* two */ asm("x // y");\nchar c = \'"\';'
+    b = 'int   a;\n\n asm("x // y"); // other\nchar c = \'"\'; /* */'
+    assert bench._code_only(a) == bench._code_only(b) == 'int a; asm("x // y"); char c = \'"\';'
+    assert bench._code_only(a) != bench._code_only(a.replace("int a", "int b"))
+    for key, ent in bench.NCU_TRAFFIC.items():
+        assert len(ent["sources_sha256"]) == 64 and ent["bytes"] > 0
