@@ -70,7 +70,7 @@ typedef enum {
                                   block, also prepared, are added by the same CTA. Sum and
                                   mean, N % 16 == 0, aligned B and C, a plan of whole rows
                                   (not a row range)                                          */
-    SPMM_FAMILY_SEGMENT = 5    /* skewed graphs without column locality: the CSR traversal is
+    SPMM_FAMILY_SEGMENT = 5,   /* skewed graphs without column locality: the CSR traversal is
                                   cut into equal merge-path tiles of entries plus row ends
                                   (ParamSpMM section 3.2, nonzero-split balancing); each warp
                                   streams its tiles' rowptr/col/val into shared memory with
@@ -79,6 +79,16 @@ typedef enum {
                                   at the ends of a warp's range combined by a second launch.
                                   N % 4 == 0, 16-byte aligned B, C, argmax, col and val;
                                   long rows need no separate split                          */
+    SPMM_FAMILY_GATHER = 6     /* skewed graphs at wide N: equal contiguous entry ranges, one
+                                  per CTA; a producer warp streams the range's col/val and
+                                  the plan's per-entry row ids and has the tensor-copy engine
+                                  gather the entries' B rows (tile::gather4, four rows per
+                                  copy) into a shared-memory ring; four consumer warps own a
+                                  quarter of the column tile each and walk the entries in
+                                  CSR order. The rows open at the ends of a CTA's range are
+                                  combined by a second launch. N % 128 == 0, 16-byte aligned
+                                  B, C and argmax; the row ids (4 bytes per entry) are built
+                                  at the plan's first GATHER run                            */
 } spmm_family;
 
 typedef struct spmm_plan_s *spmm_plan_t;
@@ -130,6 +140,11 @@ typedef struct {
     /* BLOCK family: device bytes of the plan's prepared diagonal blocks and
        off-block entries (0 until prepared) */
     int64_t block_bytes;
+    /* GATHER family: device bytes of the plan's per-entry row ids (0 until its
+       first run), and for the queried (N, reduce) the CTAs per column tile */
+    int64_t gather_bytes;
+    int32_t gather_ctas;
+    int32_t gather_pad;     /* zero */
 } spmm_plan_info;
 
 /*

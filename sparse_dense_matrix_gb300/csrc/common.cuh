@@ -72,6 +72,11 @@ struct Plan {
     int64_t bk_n_off = 0, bk_bytes = 0;
     int bk_flavor = -1;
 
+    // GATHER family, built at its first run (gather_prepare): the row id of
+    // every stored entry, [nnz]
+    int32_t *ga_rid = nullptr;
+    int64_t ga_bytes = 0;
+
     int32_t *err = nullptr;          // device error words, see kErr*
     int family_override = SPMM_FAMILY_AUTO;
 
@@ -148,6 +153,8 @@ struct RunArgs {
     const int32_t *__restrict__ bk_off_col;
     const float *__restrict__ bk_off_val;
     float *bk_p;                              // [M][N] off-block partial rows (workspace)
+    // GATHER family (the plan's per-entry row ids; its open rows use seg_*)
+    const int32_t *__restrict__ ga_rid;
 };
 
 // Fused epilogue on V consecutive outputs starting at column c: C = act(C + bias).
@@ -328,6 +335,16 @@ cudaError_t launch_segment(const RunArgs &a, int lanes, int chunks, int reduce, 
 size_t segment_workspace(int64_t seg_warps, int64_t tiles_y, int lanes, int chunks, int reduce);
 // warps of a SEGMENT launch on `num_sms` SMs with `tiles_y` column tiles
 int64_t segment_warps(int64_t n_tiles, int num_sms, int64_t tiles_y);
+// GATHER: column tile (256 or 128 columns, 0 if N fits neither), CTAs of a
+// launch, open-row workspace bytes, the per-entry row ids (once per plan),
+// and the launch of the main kernel plus the open-row combine
+int gather_tile(int64_t N);
+int64_t gather_ctas(int64_t nnz, int num_sms, int64_t tiles_y);
+size_t gather_workspace(int64_t ctas, int64_t tiles_y, int ct, int reduce);
+cudaError_t gather_prepare(Plan *p, cudaStream_t s);
+void gather_free(Plan *p);
+cudaError_t launch_gather(const RunArgs &a, int reduce, bool has_val, int ctas, int tiles_y,
+                          cudaStream_t s);
 // grow a plan's workspace to at least `need` bytes (cudaMalloc; synchronous)
 spmm_status plan_ensure_workspace(Plan *p, size_t need);
 

@@ -1,0 +1,7 @@
+// GATHER family, sum instantiation (see gather.cuh).
+#include "gather.cuh"
+
+namespace spmm {
+template cudaError_t launch_gather_red<SPMM_SUM>(const RunArgs &, const CUtensorMap &, int, bool,
+                                                 int, int, cudaStream_t);
+}  // namespace spmm

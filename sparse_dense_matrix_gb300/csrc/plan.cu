@@ -365,6 +365,7 @@ void destroy(Plan *p) {
     if (!p) return;
     free_heavy(p);
     block_free(p);
+    gather_free(p);
     dev_free(p->seg_tiles);
     dev_free(p->rowptr);
     dev_free(p->work);
@@ -430,6 +431,8 @@ spmm_status plan_ensure_workspace(Plan *p, size_t need) { return ensure_workspac
 //       tiles (COLTILE, the staged variant, measured 1.1-1.7x slower: pin only);
 //   R3  skewed degrees (CV_d > 1), N <= 32 in 128-bit vectors, col/val
 //       16-byte aligned                                       -> SEGMENT (merge-path tiles);
+//       (GATHER, TMA gather4 of B rows into a shared ring, N % 128 == 0:
+//       pin only)
 //   R4  near-uniform degrees (CV_d <= 1) and narrow N (L < 32 lanes, so
 //       several rows share a warp)                            -> ROWGROUP, 32/L rows per warp;
 //   R5  otherwise (skewed degrees)                            -> WARPROW.
@@ -513,11 +516,17 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     // SEGMENT needs 128-bit vectors and col/val that bulk copies may read
     // (16-byte aligned)
     const bool segment_ok = o->vec == 4 && (aligned & 2) && d->M > 0 && d->seg_tiles > 0;
+    // GATHER needs column tiles of 256 or 128 columns that the gathered rows
+    // fill exactly (N % 128 == 0), 16-byte aligned B (its tensor map), C and
+    // argmax, and at least one entry
+    const bool gather_ok = (aligned & 1) && gather_tile(N) > 0 && d->M > 0 && d->nnz > 0;
     if (fam == -2) {
         if (family_override == SPMM_FAMILY_COLTILE)
             fam = coltile_ok ? SPMM_FAMILY_COLTILE : SPMM_FAMILY_WARPROW;
         else if (family_override == SPMM_FAMILY_SEGMENT)
             fam = segment_ok ? SPMM_FAMILY_SEGMENT : SPMM_FAMILY_WARPROW;
+        else if (family_override == SPMM_FAMILY_GATHER)
+            fam = gather_ok ? SPMM_FAMILY_GATHER : SPMM_FAMILY_WARPROW;
         else if (family_override != SPMM_FAMILY_AUTO && family_override != SPMM_FAMILY_WINDOW &&
                  family_override != SPMM_FAMILY_BLOCK)
             fam = family_override;
@@ -543,15 +552,26 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     // is wider than 128 columns, column tiles of 256 beyond that
     const int64_t seg_q = n_vec > 32 ? 2 : 1;
     o->lanes = (int32_t)lanes;
-    if (fam == SPMM_FAMILY_BLOCK) lanes = 32;
+    if (fam == SPMM_FAMILY_BLOCK || fam == SPMM_FAMILY_GATHER) lanes = 32;
     o->col_tiles = fam == SPMM_FAMILY_WINDOW    ? (int32_t)win_tiles
                    : fam == SPMM_FAMILY_BLOCK   ? (int32_t)((N + 127) / 128)
+                   : fam == SPMM_FAMILY_GATHER  ? (int32_t)(N / gather_tile(N))
                    : fam == SPMM_FAMILY_SEGMENT ? (int32_t)((n_vec + lanes * seg_q - 1) / (lanes * seg_q))
                                                 : (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
     o->family = fam;
     o->rows_per_warp = fam == SPMM_FAMILY_ROWGROUP ? (int32_t)(32 / lanes) : 1;
     o->seg_warps = 0;
     o->seg_chunks = 0;
+    o->gather_ctas = 0;
+    o->gather_pad = 0;
+    if (fam == SPMM_FAMILY_GATHER) {
+        // every row, however long, goes through the entry ranges: no split
+        o->gather_ctas = (int32_t)gather_ctas(d->nnz, num_sms, o->col_tiles);
+        o->launches = 2;
+        o->workspace_bytes =
+            (int64_t)gather_workspace(o->gather_ctas, o->col_tiles, gather_tile(N), reduce);
+        return;
+    }
     if (fam == SPMM_FAMILY_BLOCK) {
         // the off-block partial rows, [M][N] fp32
         o->launches = (d->M > 0 && N > 0) ? 1 : 0;
@@ -595,7 +615,7 @@ spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce
                        int num_sms, int family_override, spmm_plan_info *out) {
     if (!desc || !out || N < 0) return SPMM_ERR_INVALID_ARG;
     if (reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
-    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_SEGMENT)
+    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_GATHER)
         return SPMM_ERR_INVALID_ARG;
     route_fill(desc, N, reduce, aligned, num_sms, family_override, out);
     return SPMM_OK;
@@ -752,6 +772,7 @@ static void fill_desc(const Plan *p, spmm_plan_info *o) {
     o->row0 = p->row0;
     o->seg_tiles = p->seg_n_tiles;
     o->block_bytes = p->bk_bytes;
+    o->gather_bytes = p->ga_bytes;
 }
 
 spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce, spmm_plan_info *out) {
@@ -763,7 +784,7 @@ spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce, 
 }
 
 spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split) {
-    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_SEGMENT) return SPMM_ERR_INVALID_ARG;
+    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_GATHER) return SPMM_ERR_INVALID_ARG;
     Plan *p = reinterpret_cast<Plan *>(plan);
     p->family_override = family;
     // The kernels compare row lengths against a 32-bit threshold; no row is
@@ -788,7 +809,15 @@ spmm_status spmm_plan_reserve(spmm_plan_t plan, int64_t N, spmm_reduce reduce) {
     fill_desc(p, &r);
     route_fill(&r, N, reduce, 7, p->num_sms, p->family_override, &r);
     const size_t blk = r.family == SPMM_FAMILY_BLOCK ? (size_t)r.workspace_bytes : 0;
-    return ensure_workspace(p, std::max(std::max(workspace_need(p, N, reduce), seg), blk));
+    // and the GATHER family's open rows and per-entry row ids when routed
+    const size_t gat = r.family == SPMM_FAMILY_GATHER ? (size_t)r.workspace_bytes : 0;
+    if (r.family == SPMM_FAMILY_GATHER && !p->ga_rid) {
+        cudaError_t e = gather_prepare(p, nullptr);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    return ensure_workspace(
+        p, std::max(std::max(workspace_need(p, N, reduce), seg), std::max(blk, gat)));
 }
 
 spmm_status spmm_plan_validate_cols(spmm_plan_t plan, const int32_t *col, void *stream) {
@@ -921,6 +950,24 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
     a.row0 = p->row0;
     a.seg_tiles = p->seg_tiles;
     a.seg_n_tiles = p->seg_n_tiles;
+    if (r.family == SPMM_FAMILY_GATHER) {
+        // the per-entry row ids are built once per plan, on the first GATHER run
+        if (!p->ga_rid) {
+            cudaError_t e = gather_prepare(p, s);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+        spmm_status st = ensure_workspace(p, (size_t)r.workspace_bytes);
+        if (st != SPMM_OK) return st;
+        a.ga_rid = p->ga_rid;
+        char *wb = reinterpret_cast<char *>(p->work);
+        const size_t meta = ((size_t)r.gather_ctas * sizeof(int4) + 255) / 256 * 256;
+        const size_t vals = (size_t)r.col_tiles * (size_t)r.gather_ctas * 2 *
+                            (size_t)gather_tile(N) * 4;
+        a.seg_meta = reinterpret_cast<int4 *>(wb);
+        a.seg_cval = reinterpret_cast<float *>(wb + meta);
+        a.seg_carg = reduce == SPMM_MAX ? reinterpret_cast<int32_t *>(wb + meta + vals) : nullptr;
+        return from_cuda(launch_gather(a, reduce, val != nullptr, r.gather_ctas, r.col_tiles, s));
+    }
     if (r.family == SPMM_FAMILY_SEGMENT) {
         spmm_status st = ensure_workspace(p, (size_t)r.workspace_bytes);
         if (st != SPMM_OK) return st;

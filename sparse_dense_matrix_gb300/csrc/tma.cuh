@@ -150,4 +150,18 @@ __device__ __forceinline__ void tensor2d_g2s(void *dst, const CUtensorMap *map, 
         : "memory");
 }
 
+// Four rows of a 2-D tensor, each one box row of the tensor map (whose box is
+// one row high) from column x, into consecutive box rows of this CTA's shared
+// memory (128-byte aligned), completing on `bar` (tile::gather4). Rows outside
+// the tensor are filled with zeros.
+__device__ __forceinline__ void gather4_g2s(void *dst, const CUtensorMap *map, int x, int r0,
+                                            int r1, int r2, int r3, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1),
+          "r"(r2), "r"(r3), "r"(smem_addr(bar))
+        : "memory");
+}
+
 }  // namespace spmm

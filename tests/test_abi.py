@@ -148,6 +148,30 @@ def test_router_segment_rule(sdm):
     assert sdm.spmm_route(d, 6, 0, aligned=3, family=pin)["family_name"] == "warprow"
 
 
+def test_router_gather_rule(sdm):
+    """Pinned GATHER: column tiles of 256 (else 128) columns that N fills
+    exactly, two CTAs per SM shared among the tiles but never more CTAs than
+    entries, two launches, no split-row launches, a workspace of two partial
+    rows per CTA (+ a 16-byte record per CTA, rounded to 256 bytes)."""
+    pin = sdm.FAMILY["gather"]
+    d = _desc(M=1 << 22, nnz=104_839_949, cv=20.6, n_heavy=9000, n_chunks=90000)
+    r = sdm.spmm_route(d, 256, 0, aligned=3, family=pin)
+    assert (r["family_name"], r["col_tiles"], r["gather_ctas"], r["launches"]) == \
+        ("gather", 1, 304, 2)
+    assert r["workspace_bytes"] == 304 * 16 + 304 * 2 * 256 * 4
+    r = sdm.spmm_route(d, 256, 2, aligned=1, family=pin)       # + argmax partials
+    assert r["workspace_bytes"] == 304 * 16 + 2 * 304 * 2 * 256 * 4
+    r = sdm.spmm_route(d, 384, 0, aligned=1, family=pin)       # three tiles of 128
+    assert (r["family_name"], r["col_tiles"], r["gather_ctas"]) == ("gather", 3, 101)
+    assert r["workspace_bytes"] == (101 * 16 + 255) // 256 * 256 + 3 * 101 * 2 * 128 * 4
+    r = sdm.spmm_route(d, 512, 0, aligned=1, family=pin)       # two tiles of 256
+    assert (r["col_tiles"], r["gather_ctas"]) == (2, 152)
+    r = sdm.spmm_route(_desc(M=5, nnz=6), 128, 0, aligned=1, family=pin)
+    assert (r["family_name"], r["gather_ctas"]) == ("gather", 6)   # one CTA per entry
+    for N, aligned, dd in ((64, 3, d), (130, 3, d), (256, 2, d), (256, 3, _desc(nnz=0))):
+        assert sdm.spmm_route(dd, N, 0, aligned=aligned, family=pin)["family_name"] != "gather"
+
+
 def test_router_split_launches_and_workspace(sdm):
     r = sdm.spmm_route(_desc(cv=9.0, n_heavy=3, n_chunks=40), 64, 0)
     assert r["launches"] == 3 and r["workspace_bytes"] == 40 * 64 * 4
