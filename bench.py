@@ -71,6 +71,9 @@ FAMILY_SOURCES = {
                 _CSRC + "f_segment.cu", _CSRC + "f_segment_sum.cu", _CSRC + "f_segment_max.cu",
                 "include/spmm.h"),
     "block": (_CSRC + "common.cuh", _CSRC + "tma.cuh", _CSRC + "f_block.cu", "include/spmm.h"),
+    "stream": (_CSRC + "common.cuh", _CSRC + "segment.cuh", _CSRC + "stream.cuh",
+               _CSRC + "f_stream.cu", _CSRC + "f_stream_sum.cu", _CSRC + "f_stream_max.cu",
+               "include/spmm.h"),
     "gather": (_CSRC + "common.cuh", _CSRC + "tma.cuh", _CSRC + "segment.cuh",
                _CSRC + "gather.cuh", _CSRC + "f_gather.cu", _CSRC + "f_gather_sum.cu",
                _CSRC + "f_gather_max.cu", "include/spmm.h"),
@@ -136,7 +139,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--family", default="auto",
                     choices=["auto", "rowgroup", "warprow", "coltile", "window", "block",
-                             "segment", "gather"])
+                             "segment", "gather", "stream"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds of oracle work for the whole --impl reference run")

@@ -79,7 +79,7 @@ typedef enum {
                                   at the ends of a warp's range combined by a second launch.
                                   N % 4 == 0, 16-byte aligned B, C, argmax, col and val;
                                   long rows need no separate split                          */
-    SPMM_FAMILY_GATHER = 6     /* skewed graphs at wide N: equal contiguous entry ranges, one
+    SPMM_FAMILY_GATHER = 6,    /* skewed graphs at wide N: equal contiguous entry ranges, one
                                   per CTA; a producer warp streams the range's col/val and
                                   the plan's per-entry row ids and has the tensor-copy engine
                                   gather the entries' B rows (tile::gather4, four rows per
@@ -89,6 +89,14 @@ typedef enum {
                                   combined by a second launch. N % 128 == 0, 16-byte aligned
                                   B, C and argmax; the row ids (4 bytes per entry) are built
                                   at the plan's first GATHER run                            */
+    SPMM_FAMILY_STREAM = 7     /* skewed graphs at N > 32: the entries as one stream cut into
+                                  equal contiguous ranges, one per lane group (16 lanes for
+                                  N <= 64, else 32 per 128-column tile); each group loads the
+                                  columns, values and per-entry row ids of its next 32
+                                  entries while gathering the current ones, and finishes a
+                                  row when the row id changes. The rows open at the ends of
+                                  a range are combined by a second launch. N % 4 == 0,
+                                  16-byte aligned B, C and argmax; shares GATHER's row ids */
 } spmm_family;
 
 typedef struct spmm_plan_s *spmm_plan_t;
@@ -144,7 +152,8 @@ typedef struct {
        first run), and for the queried (N, reduce) the CTAs per column tile */
     int64_t gather_bytes;
     int32_t gather_ctas;
-    int32_t gather_pad;     /* zero */
+    /* STREAM family: for the queried (N, reduce) the entry ranges of the grid */
+    int32_t stream_ranges;
 } spmm_plan_info;
 
 /*

@@ -39,7 +39,7 @@ __all__ = [
 REDUCE = {"sum": 0, "mean": 1, "max": 2}
 ACT = {None: 0, "none": 0, "relu": 1}
 FAMILY = {"auto": -1, "rowgroup": 0, "warprow": 1, "coltile": 2, "window": 3, "block": 4,
-          "segment": 5, "gather": 6}
+          "segment": 5, "gather": 6, "stream": 7}
 STATUS = {0: "SPMM_OK", 1: "SPMM_ERR_INVALID_ARG", 2: "SPMM_ERR_INVALID_INPUT", 3: "SPMM_ERR_OOM",
           4: "SPMM_ERR_CUDA", 5: "SPMM_ERR_UNSUPPORTED", 6: "SPMM_ERR_TIMEOUT"}
 
@@ -63,7 +63,7 @@ class PlanInfo(ctypes.Structure):
         ("seg_tiles", ctypes.c_int64), ("seg_warps", ctypes.c_int32),
         ("seg_chunks", ctypes.c_int32), ("block_bytes", ctypes.c_int64),
         ("gather_bytes", ctypes.c_int64), ("gather_ctas", ctypes.c_int32),
-        ("gather_pad", ctypes.c_int32),
+        ("stream_ranges", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -20,7 +20,8 @@ LIB = os.path.join(PKG, "libspmm.so")
 SOURCES = ["plan.cu", "f_rowgroup.cu", "f_warprow.cu", "f_window.cu", "f_window_sum.cu",
            "f_window_mean.cu", "f_window_max.cu", "f_coltile.cu", "noalloc.cu",
            "transpose.cu", "f_block.cu", "selftest.cu", "f_segment.cu", "f_segment_sum.cu",
-           "f_segment_max.cu", "f_gather.cu", "f_gather_sum.cu", "f_gather_max.cu"]
+           "f_segment_max.cu", "f_gather.cu", "f_gather_sum.cu", "f_gather_max.cu",
+           "f_stream.cu", "f_stream_sum.cu", "f_stream_max.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

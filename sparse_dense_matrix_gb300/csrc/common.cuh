@@ -345,6 +345,14 @@ cudaError_t gather_prepare(Plan *p, cudaStream_t s);
 void gather_free(Plan *p);
 cudaError_t launch_gather(const RunArgs &a, int reduce, bool has_val, int ctas, int tiles_y,
                           cudaStream_t s);
+// STREAM: lanes per range (16 or 32; 0 when N % 4 != 0 or N <= 32), ranges of
+// a launch, open-row workspace bytes, and the launch of the main kernel plus
+// the open-row combine (the per-entry row ids come from gather_prepare)
+int stream_lanes(int64_t N);
+int64_t stream_ranges(int64_t nnz, int num_sms, int lanes, int64_t tiles_y);
+size_t stream_workspace(int64_t ranges, int64_t tiles_y, int lanes, int reduce);
+cudaError_t launch_stream(const RunArgs &a, int reduce, bool has_val, int lanes, int64_t ranges,
+                          int tiles_y, cudaStream_t s);
 // grow a plan's workspace to at least `need` bytes (cudaMalloc; synchronous)
 spmm_status plan_ensure_workspace(Plan *p, size_t need);
 

@@ -520,6 +520,9 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     // fill exactly (N % 128 == 0), 16-byte aligned B (its tensor map), C and
     // argmax, and at least one entry
     const bool gather_ok = (aligned & 1) && gather_tile(N) > 0 && d->M > 0 && d->nnz > 0;
+    // STREAM needs 128-bit vectors (N % 4 == 0, aligned B/C/argmax), N > 32
+    // and at least one entry
+    const bool stream_ok = o->vec == 4 && stream_lanes(N) > 0 && d->M > 0 && d->nnz > 0;
     if (fam == -2) {
         if (family_override == SPMM_FAMILY_COLTILE)
             fam = coltile_ok ? SPMM_FAMILY_COLTILE : SPMM_FAMILY_WARPROW;
@@ -527,6 +530,8 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
             fam = segment_ok ? SPMM_FAMILY_SEGMENT : SPMM_FAMILY_WARPROW;
         else if (family_override == SPMM_FAMILY_GATHER)
             fam = gather_ok ? SPMM_FAMILY_GATHER : SPMM_FAMILY_WARPROW;
+        else if (family_override == SPMM_FAMILY_STREAM)
+            fam = stream_ok ? SPMM_FAMILY_STREAM : SPMM_FAMILY_WARPROW;
         else if (family_override != SPMM_FAMILY_AUTO && family_override != SPMM_FAMILY_WINDOW &&
                  family_override != SPMM_FAMILY_BLOCK)
             fam = family_override;
@@ -551,11 +556,13 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     // SEGMENT: L lanes x Q four-column chunks per lane; two chunks when a row
     // is wider than 128 columns, column tiles of 256 beyond that
     const int64_t seg_q = n_vec > 32 ? 2 : 1;
+    if (fam == SPMM_FAMILY_STREAM) lanes = stream_lanes(N);
     o->lanes = (int32_t)lanes;
     if (fam == SPMM_FAMILY_BLOCK || fam == SPMM_FAMILY_GATHER) lanes = 32;
     o->col_tiles = fam == SPMM_FAMILY_WINDOW    ? (int32_t)win_tiles
                    : fam == SPMM_FAMILY_BLOCK   ? (int32_t)((N + 127) / 128)
                    : fam == SPMM_FAMILY_GATHER  ? (int32_t)(N / gather_tile(N))
+                   : fam == SPMM_FAMILY_STREAM  ? (int32_t)((n_vec + lanes - 1) / lanes)
                    : fam == SPMM_FAMILY_SEGMENT ? (int32_t)((n_vec + lanes * seg_q - 1) / (lanes * seg_q))
                                                 : (int32_t)std::max<int64_t>(1, (n_vec + lanes - 1) / lanes);
     o->family = fam;
@@ -563,7 +570,15 @@ static void route_fill(const spmm_plan_info *d, int64_t N, int reduce, int align
     o->seg_warps = 0;
     o->seg_chunks = 0;
     o->gather_ctas = 0;
-    o->gather_pad = 0;
+    o->stream_ranges = 0;
+    if (fam == SPMM_FAMILY_STREAM) {
+        // every row, however long, goes through the entry ranges: no split
+        o->stream_ranges = (int32_t)stream_ranges(d->nnz, num_sms, (int)lanes, o->col_tiles);
+        o->launches = 2;
+        o->workspace_bytes =
+            (int64_t)stream_workspace(o->stream_ranges, o->col_tiles, (int)lanes, reduce);
+        return;
+    }
     if (fam == SPMM_FAMILY_GATHER) {
         // every row, however long, goes through the entry ranges: no split
         o->gather_ctas = (int32_t)gather_ctas(d->nnz, num_sms, o->col_tiles);
@@ -615,7 +630,7 @@ spmm_status spmm_route(const spmm_plan_info *desc, int64_t N, spmm_reduce reduce
                        int num_sms, int family_override, spmm_plan_info *out) {
     if (!desc || !out || N < 0) return SPMM_ERR_INVALID_ARG;
     if (reduce < SPMM_SUM || reduce > SPMM_MAX) return SPMM_ERR_INVALID_ARG;
-    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_GATHER)
+    if (family_override < SPMM_FAMILY_AUTO || family_override > SPMM_FAMILY_STREAM)
         return SPMM_ERR_INVALID_ARG;
     route_fill(desc, N, reduce, aligned, num_sms, family_override, out);
     return SPMM_OK;
@@ -784,7 +799,7 @@ spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce, 
 }
 
 spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split) {
-    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_GATHER) return SPMM_ERR_INVALID_ARG;
+    if (!plan || family < SPMM_FAMILY_AUTO || family > SPMM_FAMILY_STREAM) return SPMM_ERR_INVALID_ARG;
     Plan *p = reinterpret_cast<Plan *>(plan);
     p->family_override = family;
     // The kernels compare row lengths against a 32-bit threshold; no row is
@@ -810,8 +825,9 @@ spmm_status spmm_plan_reserve(spmm_plan_t plan, int64_t N, spmm_reduce reduce) {
     route_fill(&r, N, reduce, 7, p->num_sms, p->family_override, &r);
     const size_t blk = r.family == SPMM_FAMILY_BLOCK ? (size_t)r.workspace_bytes : 0;
     // and the GATHER family's open rows and per-entry row ids when routed
-    const size_t gat = r.family == SPMM_FAMILY_GATHER ? (size_t)r.workspace_bytes : 0;
-    if (r.family == SPMM_FAMILY_GATHER && !p->ga_rid) {
+    const bool rows_ids = r.family == SPMM_FAMILY_GATHER || r.family == SPMM_FAMILY_STREAM;
+    const size_t gat = rows_ids ? (size_t)r.workspace_bytes : 0;
+    if (rows_ids && !p->ga_rid) {
         cudaError_t e = gather_prepare(p, nullptr);
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
         if (e != cudaSuccess) return from_cuda(e);
@@ -950,6 +966,25 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
     a.row0 = p->row0;
     a.seg_tiles = p->seg_tiles;
     a.seg_n_tiles = p->seg_n_tiles;
+    if (r.family == SPMM_FAMILY_STREAM) {
+        // the per-entry row ids are built once per plan, on its first run
+        if (!p->ga_rid) {
+            cudaError_t e = gather_prepare(p, s);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+        spmm_status st = ensure_workspace(p, (size_t)r.workspace_bytes);
+        if (st != SPMM_OK) return st;
+        a.ga_rid = p->ga_rid;
+        char *wb = reinterpret_cast<char *>(p->work);
+        const size_t meta = ((size_t)r.stream_ranges * sizeof(int4) + 255) / 256 * 256;
+        const size_t vals = (size_t)r.col_tiles * (size_t)r.stream_ranges * 2 * 4 *
+                            (size_t)r.lanes * 4;
+        a.seg_meta = reinterpret_cast<int4 *>(wb);
+        a.seg_cval = reinterpret_cast<float *>(wb + meta);
+        a.seg_carg = reduce == SPMM_MAX ? reinterpret_cast<int32_t *>(wb + meta + vals) : nullptr;
+        return from_cuda(launch_stream(a, reduce, val != nullptr, r.lanes, r.stream_ranges,
+                                       r.col_tiles, s));
+    }
     if (r.family == SPMM_FAMILY_GATHER) {
         // the per-entry row ids are built once per plan, on the first GATHER run
         if (!p->ga_rid) {

@@ -172,6 +172,29 @@ def test_router_gather_rule(sdm):
         assert sdm.spmm_route(dd, N, 0, aligned=aligned, family=pin)["family_name"] != "gather"
 
 
+def test_router_stream_rule(sdm):
+    """Pinned STREAM: 16 lanes per range up to N = 64, else 32 lanes per
+    128-column tile; two waves of 4 x 256-thread blocks per SM shared among
+    the tiles, 32 / lanes ranges per warp, at least 16 entries a range; two
+    launches, no split-row launches, a workspace of two partial rows per range
+    (+ a 16-byte record per range, rounded to 256 bytes)."""
+    pin = sdm.FAMILY["stream"]
+    d = _desc(M=1 << 22, nnz=104_839_949, cv=20.6, n_heavy=9000, n_chunks=90000)
+    r = sdm.spmm_route(d, 64, 0, aligned=3, family=pin)
+    assert (r["family_name"], r["lanes"], r["col_tiles"], r["stream_ranges"], r["launches"]) == \
+        ("stream", 16, 1, 19456, 2)
+    assert r["workspace_bytes"] == 19456 * 16 + 19456 * 2 * 64 * 4
+    r = sdm.spmm_route(d, 256, 2, aligned=1, family=pin)       # + argmax partials
+    assert (r["lanes"], r["col_tiles"], r["stream_ranges"]) == (32, 2, 4864)
+    assert r["workspace_bytes"] == 4864 * 16 + 2 * 2 * 4864 * 2 * 128 * 4
+    r = sdm.spmm_route(d, 48, 0, aligned=1, family=pin)        # 12 of 16 lanes active
+    assert (r["family_name"], r["lanes"], r["col_tiles"]) == ("stream", 16, 1)
+    r = sdm.spmm_route(_desc(M=5, nnz=6), 128, 0, aligned=1, family=pin)
+    assert (r["family_name"], r["stream_ranges"]) == ("stream", 1)
+    for N, aligned, dd in ((32, 3, d), (66, 3, d), (256, 2, d), (256, 3, _desc(nnz=0))):
+        assert sdm.spmm_route(dd, N, 0, aligned=aligned, family=pin)["family_name"] != "stream"
+
+
 def test_router_split_launches_and_workspace(sdm):
     r = sdm.spmm_route(_desc(cv=9.0, n_heavy=3, n_chunks=40), 64, 0)
     assert r["launches"] == 3 and r["workspace_bytes"] == 40 * 64 * 4
