@@ -238,11 +238,12 @@ spmm_status spmm_partition_rows(const int32_t *rowptr, int64_t M, int32_t parts,
  *   argmax : device, int32 [M, N] (SPMM_MAX only; may be NULL to skip it).
  * 128-bit loads are used when N % 4 == 0 and B and C are 16-byte aligned;
  * otherwise the scalar path runs (same results). Grows the plan's workspace
- * with cudaMalloc when the heavy-row split or the SEGMENT family's open rows
- * need more than it holds (use spmm_plan_reserve beforehand to keep
- * allocation out of timed or captured regions), and the first BLOCK product
- * prepares the plan's diagonal blocks (spmm_plan_prepare_blocks beforehand
- * does the same).
+ * with cudaMalloc when the heavy-row split or the open rows of the SEGMENT,
+ * GATHER or STREAM families need more than it holds; the first GATHER or
+ * STREAM product builds the plan's per-entry row ids (4 bytes per entry); use
+ * spmm_plan_reserve beforehand to keep both out of timed or captured
+ * regions. The first BLOCK product prepares the plan's diagonal blocks
+ * (spmm_plan_prepare_blocks beforehand does the same).
  * (ParamSpMM section 2, Algorithm 1; graph-spmm model card, "Method".)
  */
 spmm_status spmm_run(spmm_plan_t plan, const int32_t *col, const float *val, const float *B,
@@ -269,7 +270,9 @@ spmm_status spmm_run_ex(spmm_plan_t plan, const int32_t *col, const float *val, 
 
 /*
  * spmm_plan_reserve -- allocate the workspace spmm_run needs for (N, reduce)
- * now. Synchronous (cudaMalloc). Returns SPMM_ERR_OOM on failure.
+ * now, and when that product goes to the GATHER or STREAM family, build the
+ * plan's per-entry row ids. Synchronous (cudaMalloc). Returns SPMM_ERR_OOM on
+ * failure.
  */
 spmm_status spmm_plan_reserve(spmm_plan_t plan, int64_t N, spmm_reduce reduce);
 
