@@ -149,6 +149,25 @@ def test_stream_row_ids_built_once(sdm, cuda_device):
     adj.close()
 
 
+def test_stream_reserve_builds_row_ids(sdm, cuda_device):
+    """spmm_plan_reserve for a product routed to STREAM builds the row ids up
+    front, so the first product allocates nothing more."""
+    import torch
+    g = graph("chung_lu")
+    B = gen.features(g.K, 64, seed=4)
+    Bd = to_dev(B, cuda_device)
+    adj, info = stream_adj(sdm, g, cuda_device, 64, "max")
+    assert info["gather_bytes"] == 0
+    adj.reserve(64, "max")
+    assert adj.describe(64, "max")["gather_bytes"] == 4 * g.nnz
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    C, A = gpu_reduce(adj, Bd, "max")
+    assert torch.cuda.mem_get_info()[0] >= free0 - (64 << 20)   # outputs only, no workspace
+    compare(g, B, "max", C, A, label="stream after reserve")
+    adj.close()
+
+
 def test_stream_epilogue(sdm, cuda_device):
     import torch
 
