@@ -327,14 +327,18 @@ spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce,
  * the router) and the heavy-row threshold (t_split <= 0 restores the default;
  * a threshold above INT32_MAX is taken as INT32_MAX, i.e. no row is split;
  * a new threshold rebuilds the heavy-row tables, synchronously on the legacy
- * default stream). For tests and benchmarks of individual families.
+ * default stream). `family` is an spmm_family value, SPMM_FAMILY_AUTO to
+ * SPMM_FAMILY_STREAM, else SPMM_ERR_INVALID_ARG; a pinned family whose
+ * conditions (see spmm_family) do not hold for a product runs that product
+ * as WARPROW. For tests and benchmarks of individual families.
  */
 spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split);
 
 /*
  * spmm_route -- the router as a pure host function. Reads the descriptor
  * fields of *desc (M, K, nnz, d_max, dbar, cv, t_split, chunk, n_heavy,
- * n_chunks, band_w, band_cover) and fills the launch-shape fields of *out for
+ * n_chunks, band_w, band_cover, blk_intra, row0, seg_tiles) and, with
+ * family_override as spmm_plan_set_family's `family`, fills the launch-shape fields of *out for
  * (N, reduce) on a GPU with `num_sms` SMs. `aligned` is a bit mask: bit 0 set
  * when B, C (and argmax) are 16-byte aligned, bit 1 set when col (and val)
  * are 16-byte aligned, bit 2 set when there is no val array (unweighted).
