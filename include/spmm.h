@@ -328,9 +328,11 @@ spmm_status spmm_plan_describe(spmm_plan_t plan, int64_t N, spmm_reduce reduce,
  * a threshold above INT32_MAX is taken as INT32_MAX, i.e. no row is split;
  * a new threshold rebuilds the heavy-row tables, synchronously on the legacy
  * default stream). `family` is an spmm_family value, SPMM_FAMILY_AUTO to
- * SPMM_FAMILY_STREAM, else SPMM_ERR_INVALID_ARG; a pinned family whose
- * conditions (see spmm_family) do not hold for a product runs that product
- * as WARPROW. For tests and benchmarks of individual families.
+ * SPMM_FAMILY_STREAM, else SPMM_ERR_INVALID_ARG. When a pinned family's
+ * conditions (see spmm_family) do not hold for a product, that product runs
+ * as WARPROW (pinned COLTILE, SEGMENT, GATHER, STREAM) or as the router
+ * would choose (pinned WINDOW, BLOCK). For tests and benchmarks of
+ * individual families.
  */
 spmm_status spmm_plan_set_family(spmm_plan_t plan, int family, int64_t t_split);
 
